@@ -1,0 +1,228 @@
+/*
+ * moe.h - C ABI of the B300 (sm_103a) library for the forward pass of one
+ * top-k routed Mixture-of-Experts FFN layer.
+ *
+ * The method (pages cited by title and section):
+ *   [MoE-math]     kwkr.cn, "MoE sparse activation: from the math to the code"
+ *                  (title lost in extraction), sections 2.1-2.3 and 3.1-3.2.
+ *   [MoE-tutorial] intelliparadigm.com, "MoE模型：动态计算架构解析与实践指南",
+ *                  sections 2.1 and 2.3.
+ *   [MoE-guide]    lpnh.cn, "Mixture of Experts（MoE）原理与工程落地全指南",
+ *                  sections 2.2, 3.2 and 3.3.
+ *
+ *   logits  l = (x W_g^T + b + g) / tau                 [MoE-math] 2.1, [MoE-guide] 3.3
+ *   probs   p = softmax(l)                               [MoE-math] 2.1
+ *   K(x)    = top-k of l, descending, ties -> lower expert index   [MoE-math] 2.1
+ *   gates   g_j = p_{K_j} / sum_m p_{K_m}               [MoE-math] 2.1
+ *   C       = ceil(c k T / E); a slot is kept iff fewer than C earlier tokens
+ *             chose the same expert (token order)       [MoE-math] 2.3, 3.2
+ *   expert  GELU:   W2 gelu(W1 x + b1) + b2              [MoE-math] 3.1
+ *           SwiGLU: W2 (silu(W1 x) * (W3 x))             ([MoE-guide] 3.2 shapes)
+ *   y_t     = sum_{kept j} g_j E_{K_j}(x_t)  (0 if every slot dropped)
+ *   f_i = count_i/(kT), P_i = mean_t p_{t,i}, L_balance = E sum_i f_i P_i
+ *                                                         [MoE-math] 2.2
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless the name ends in _host.
+ *   - Row-major, densely packed. Weights use the nn.Linear storage [out, in]:
+ *     Wg [E, d], W1 and W3 [E, H, d], W2 [E, d, H]; expert biases b1 [E, H],
+ *     b2 [E, d]. Activations x [T, d], y [T, d].
+ *   - dtype MOE_BF16: x, weights, expert biases, xd, Y, y are bf16; MOE_F32:
+ *     all fp32. Router bias, noise, logits, gates and statistics are fp32;
+ *     ids and offsets int32.
+ *   - Every device-side call only enqueues work on `stream` (a cudaStream_t)
+ *     and returns. The library never allocates, frees or synchronises, except
+ *     moe_device_status, which synchronises `stream`. The caller owns every
+ *     buffer and keeps it alive until the stream has run the work.
+ *   - Arguments are validated on the host first; on failure nothing is
+ *     enqueued and a status is returned. A failed kernel launch returns
+ *     MOE_ERR_CUDA.
+ *   - The workspace `ws` (size from moe_workspace_size, 256-byte aligned) holds
+ *     intermediates and a status header. Zero it once with moe_workspace_init
+ *     before first use; afterwards calls leave the header ready for the next
+ *     call. Calls sharing one workspace must be ordered (same stream).
+ *   - Device-detected errors (a bounded wait that ran out) are recorded in the
+ *     workspace header and read with moe_device_status.
+ *   - Limits: 1 <= k <= 8, k <= E <= 256, T >= 1, T*k < 2^31, capacity >= 1;
+ *     d and H multiples of 8 (bf16) or 4 (fp32); activations must be finite.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(MOE_BUILD_SO)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null required pointer, bad shape or limit      */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside this build (e.g. k > 8)      */
+  MOE_ERR_WORKSPACE = 3,      /* ws too small or misaligned                     */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed    */
+  MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out             */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
+
+/* Layer shape. capacity is C (see moe_capacity). tau is the router
+ * temperature (logits are divided by it; 1.0 = none). dtype and act hold a
+ * moe_dtype_t and a moe_act_t. */
+typedef struct {
+  int32_t T, d, E, k, H;
+  int32_t capacity;
+  int32_t dtype;
+  int32_t act;
+  float tau;
+} moe_config_t;
+
+/* Version of this ABI (major * 100 + minor). */
+MOE_API int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+MOE_API const char *moe_status_string(int32_t status);
+
+/* C = ceil(c k T / E) with c = c_num / c_den, in exact integer arithmetic
+ * ([MoE-math] 2.3). Host only. Returns -1 if any argument is < 1 or the
+ * result does not fit in int32. */
+MOE_API int32_t moe_capacity(int64_t c_num, int64_t c_den, int32_t k, int32_t T, int32_t E);
+
+/* Bytes of workspace every call below needs for this shape (the maximum
+ * over calls, so one workspace serves all). Host only. */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
+
+/* Zero the workspace status header (enqueued on stream). Call once after
+ * allocating a workspace, and again after a call reported an error. */
+MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Read and clear the device status word in ws. Synchronises `stream`.
+ * *code is MOE_OK, or the status a kernel recorded (MOE_ERR_DEVICE_TIMEOUT).
+ * *where identifies the waiting kernel role (0 if none). */
+MOE_API moe_status_t moe_device_status(void *ws, int32_t *code, int32_t *where,
+                               moe_stream_t stream);
+
+/* Router, softmax, top-k, renormalised gates ([MoE-math] 2.1, 3.2), one
+ * fused kernel.
+ *   x          [T, d]   input tokens (dtype)
+ *   Wg         [E, d]   router weight (dtype), nn.Linear storage
+ *   bias       [E]      fp32 router bias, or NULL
+ *   noise      [T, E]   fp32 noise added to the logits (e.g. Gumbel), or NULL
+ *   logits     [T, E]   fp32 out: the selection keys l, or NULL
+ *   topk_idx   [T, k]   int32 out: chosen experts, descending l, ties to lower id
+ *   topk_gate  [T, k]   fp32 out: renormalised gates (sum to 1 per token)
+ *   prob_sum   [E]      fp32 out: sum over tokens of p[t, e] (deterministic) */
+MOE_API moe_status_t moe_router_topk(const moe_config_t *cfg, const void *x, const void *Wg,
+                             const float *bias, const float *noise, float *logits,
+                             int32_t *topk_idx, float *topk_gate, float *prob_sum,
+                             void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Capacity-limited dispatch ([MoE-math] 2.3, 3.2): per-expert counts, a
+ * token-order position for every slot, drops beyond C, and the gather of
+ * kept rows into an expert-contiguous buffer.
+ *   topk_idx      [T, k]   int32 in
+ *   x             [T, d]   in (dtype)
+ *   expert_count  [E]      int32 out: selections per expert before drops
+ *   expert_offset [E+1]    int32 out: offset_e = sum_{e'<e} min(count_e', C)
+ *   slot_of       [T, k]   int32 out: packed row of slot (t, j), or -1 if dropped
+ *   token_of_row  [T*k]    int32 out: token of each packed row; the first
+ *                          expert_offset[E] entries are written
+ *   xd            [T*k, d] out (dtype): xd[slot_of[t,j]] = x[t]; first
+ *                          expert_offset[E] rows written */
+MOE_API moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const void *x,
+                          int32_t *expert_count, int32_t *expert_offset, int32_t *slot_of,
+                          int32_t *token_of_row, void *xd, void *ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Grouped expert FFN over the packed rows ([MoE-math] 3.1; SwiGLU for
+ * act = MOE_ACT_SWIGLU). Rows [offset_e, offset_{e+1}) of xd go through expert e.
+ *   xd            [T*k, d] in (dtype), first expert_offset[E] rows used
+ *   expert_offset [E+1]    int32 in (device; read on the device, no host sync)
+ *   W1 [E,H,d], W3 [E,H,d] (SwiGLU only, else NULL), W2 [E,d,H]   (dtype)
+ *   b1 [E,H], b2 [E,d]     GELU only, may be NULL (dtype)
+ *   Y             [T*k, d] out (dtype), first expert_offset[E] rows written.
+ * bf16 runs on the tcgen05 tensor cores with fp32 accumulation; the hidden
+ * activation h is rounded to bf16 between the two GEMMs. fp32 runs on fp32
+ * FMA. */
+MOE_API moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *xd,
+                            const int32_t *expert_offset, const void *W1, const void *W3,
+                            const void *W2, const void *b1, const void *b2, void *Y,
+                            void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gate-weighted combine ([MoE-math] 2.1, 3.2): y_t = sum over j = 0..k-1 with
+ * slot_of[t,j] >= 0 of topk_gate[t,j] * Y[slot_of[t,j]], summed in fp32 in
+ * slot order (deterministic, no atomics); y_t = 0 if every slot was dropped.
+ *   Y [T*k, d] (dtype) in, slot_of [T,k], topk_gate [T,k] in, y [T, d] out. */
+MOE_API moe_status_t moe_combine(const moe_config_t *cfg, const void *Y, const int32_t *slot_of,
+                         const float *topk_gate, void *y, moe_stream_t stream);
+
+/* Load-balance statistics ([MoE-math] 2.2, drop count per 6.2):
+ *   f[e] = expert_count[e] / (k T)   (before drops)
+ *   P[e] = prob_sum[e] / T
+ *   L_balance[0] = E * sum_e f[e] P[e]
+ *   dropped[0] = k T - sum_e min(expert_count[e], C) */
+MOE_API moe_status_t moe_aux_stats(const moe_config_t *cfg, const int32_t *expert_count,
+                           const float *prob_sum, float *f, float *P, float *L_balance,
+                           int32_t *dropped, moe_stream_t stream);
+
+/* Inputs of the fused layer call. Optional pointers may be NULL. */
+typedef struct {
+  const void *x;      /* [T, d]            */
+  const void *Wg;     /* [E, d]            */
+  const float *bias;  /* [E] or NULL       */
+  const float *noise; /* [T, E] or NULL    */
+  const void *W1;     /* [E, H, d]         */
+  const void *W3;     /* [E, H, d] or NULL */
+  const void *W2;     /* [E, d, H]         */
+  const void *b1;     /* [E, H] or NULL    */
+  const void *b2;     /* [E, d] or NULL    */
+} moe_layer_inputs_t;
+
+/* Outputs of the fused layer call. Required: y. Others may be NULL. */
+typedef struct {
+  void *y;               /* [T, d]  */
+  float *logits;         /* [T, E]  */
+  int32_t *topk_idx;     /* [T, k]  */
+  float *topk_gate;      /* [T, k]  */
+  int32_t *slot_of;      /* [T, k]  */
+  int32_t *expert_count; /* [E]     */
+  int32_t *expert_offset;/* [E+1]   */
+  float *f;              /* [E]     */
+  float *P;              /* [E]     */
+  float *L_balance;      /* [1]     */
+  int32_t *dropped;      /* [1]     */
+} moe_layer_outputs_t;
+
+/* The whole layer: router -> dispatch -> expert FFN -> combine -> statistics,
+ * enqueued on one stream with no host synchronisation. Intermediates (and any
+ * output passed as NULL) live in ws. */
+MOE_API moe_status_t moe_layer_forward(const moe_config_t *cfg, const moe_layer_inputs_t *in,
+                               const moe_layer_outputs_t *out, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/* As moe_layer_forward, but x_host [T, d] and y_host [T, d] are HOST buffers
+ * (page-locked for asynchronous copies); the weights in `in` stay on the device
+ * (in->x is ignored). The copies in and out run on `stream` inside the call's
+ * work; the caller synchronises the stream before reading y_host. If
+ * L_balance_host is not NULL the statistic is copied back too. Needs
+ * moe_workspace_size_host bytes of workspace. */
+MOE_API moe_status_t moe_workspace_size_host(const moe_config_t *cfg, size_t *bytes);
+MOE_API moe_status_t moe_layer_forward_host(const moe_config_t *cfg, const void *x_host,
+                                    const moe_layer_inputs_t *in, void *y_host,
+                                    float *L_balance_host, void *ws, size_t ws_bytes,
+                                    moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,52 @@
+"""Build the in-tree CUDA library ``libmoe_b300.so`` for sm_103a with nvcc.
+
+Usage: ``python -m mixture_experts_layer_99_b300.build`` (or ``build()``).
+The library is placed next to this file so that it travels with the source
+tree; it links the CUDA runtime statically and needs no other CUDA library at
+load time.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+LIB = os.path.join(HERE, "libmoe_b300.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+SOURCES = ["api.cu", "router.cu", "dispatch.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu"]
+
+
+def nvcc_path() -> str:
+    p = shutil.which("nvcc")
+    if p:
+        return p
+    cand = "/usr/local/cuda/bin/nvcc"
+    if os.path.exists(cand):
+        return cand
+    raise RuntimeError("nvcc not found")
+
+
+def build(verbose: bool = False, extra: list[str] | None = None) -> str:
+    srcs = [os.path.join(CSRC, s) for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
+    cmd = [nvcc_path(), "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+           "-lineinfo", *ARCH, "-cudart", "static", "-Xcompiler", "-fvisibility=hidden",
+           "-DMOE_BUILD_SO", "-I", os.path.join(HERE, "..", "include"),
+           *(extra or []), "-o", LIB + ".tmp", *srcs]
+    if verbose:
+        print(" ".join(cmd))
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("nvcc failed building libmoe_b300.so")
+    if verbose and (r.stdout or r.stderr):
+        print(r.stdout + r.stderr)
+    os.replace(LIB + ".tmp", LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(verbose="-v" in sys.argv, extra=[a for a in sys.argv[1:] if a != "-v"])
+    print(LIB)

@@ -1,0 +1,316 @@
+// The C ABI: host-side validation, workspace layout and the launch sequence of
+// each call. Every call validates first and enqueues nothing on failure.
+#include "moe_internal.h"
+
+#include <math.h>
+#include <string.h>
+
+namespace moe {
+
+WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
+  WsLayout L;
+  memset(&L, 0, sizeof(L));
+  const size_t s = elem_bytes(c);
+  const size_t T = (size_t)c.T, E = (size_t)c.E, k = (size_t)c.k;
+  const size_t R = (size_t)max_rows(c);
+  const size_t nblk = (size_t)disp_blocks(c);
+  const size_t rgrid = (size_t)router_grid(c, 0);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return at;
+  };
+  L.hdr = take(kHdrBytes);
+  L.router_partial = take(rgrid * E * 4);
+  L.disp_hist = take(nblk * E * 4);
+  L.disp_base = take(nblk * E * 4);
+  L.ffn_h = take(R * (size_t)c.H * s);
+  L.ffn_sched = take(4096);
+  L.total_core = off;
+  L.logits = take(T * E * 4);
+  L.topk_idx = take(T * k * 4);
+  L.topk_gate = take(T * k * 4);
+  L.slot_of = take(T * k * 4);
+  L.count = take(E * 4);
+  L.offset = take((E + 1) * 4);
+  L.token_of_row = take(R * 4);
+  L.xd = take(R * (size_t)c.d * s);
+  L.Y = take(R * (size_t)c.d * s);
+  L.prob_sum = take(E * 4);
+  L.f = take(E * 4);
+  L.P = take(E * 4);
+  L.L = take(4);
+  L.dropped = take(4);
+  L.total_layer = off;
+  L.x_stage = take(T * (size_t)c.d * s);
+  L.y_stage = take(T * (size_t)c.d * s);
+  L.total_host = off;
+  return L;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
+                       const void* W1, const void* W3, const void* W2, const void* b1,
+                       const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
+                       cudaStream_t s) {
+  (void)hdr;
+  return launch_ffn_simt(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d < 1 || c->E < 1 || c->k < 1 || c->H < 1 || c->capacity < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  const int align = c->dtype == MOE_F32 ? 4 : 8;
+  if (c->d % align || c->H % align) return MOE_ERR_INVALID_ARG;
+  if (!(c->tau > 0.f) || !isfinite(c->tau)) return MOE_ERR_INVALID_ARG;
+  if (c->E > kMaxE || c->k > kMaxK) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->d >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (((uintptr_t)ws) % 256) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T> T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return 100; }
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t moe_capacity(int64_t c_num, int64_t c_den, int32_t k, int32_t T, int32_t E) {
+  if (c_num < 1 || c_den < 1 || k < 1 || T < 1 || E < 1) return -1;
+  const __int128 num = (__int128)c_num * k * T;
+  const __int128 den = (__int128)c_den * E;
+  const __int128 q = (num + den - 1) / den;
+  if (q > (__int128)0x7fffffff) return -1;
+  return (int32_t)q;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*cfg, 0).total_layer;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size_host(const moe_config_t* cfg, size_t* bytes) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*cfg, 0).total_host;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  const moe_status_t st = check_ws(ws, ws_bytes, kHdrBytes);
+  if (st != MOE_OK) return st;
+  return cuda_status(cudaMemsetAsync(ws, 0, kHdrBytes, (cudaStream_t)stream));
+}
+
+moe_status_t moe_device_status(void* ws, int32_t* code, int32_t* where, moe_stream_t stream) {
+  if (!code) return MOE_ERR_INVALID_ARG;
+  const moe_status_t st = check_ws(ws, kHdrBytes, kHdrBytes);
+  if (st != MOE_OK) return st;
+  int32_t h[2] = {0, 0};
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(h), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *code = h[kHdrStatus];
+  if (where) *where = h[kHdrWhere];
+  return MOE_OK;
+}
+
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* Wg,
+                             const float* bias, const float* noise, float* logits,
+                             int32_t* topk_idx, float* topk_gate, float* prob_sum, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !topk_idx || !topk_gate || !prob_sum) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total_core)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int grid = router_grid(*cfg, 0);
+  float* partial = at<float>(ws, L.router_partial);
+  cudaError_t e = launch_router(*cfg, x, Wg, bias, noise, logits, topk_idx, topk_gate,
+                                partial, grid, s);
+  if (e == cudaSuccess) e = launch_prob_reduce(*cfg, partial, grid, prob_sum, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, const void* x,
+                          int32_t* expert_count, int32_t* expert_offset, int32_t* slot_of,
+                          int32_t* token_of_row, void* xd, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !x || !expert_count || !expert_offset || !slot_of || !token_of_row || !xd)
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total_core)) != MOE_OK) return st;
+  return cuda_status(launch_dispatch(*cfg, topk_idx, x, expert_count, expert_offset, slot_of,
+                                     token_of_row, xd, at<int32_t>(ws, L.disp_hist),
+                                     at<int32_t>(ws, L.disp_base),
+                                     (int64_t)cfg->T * cfg->k, (cudaStream_t)stream));
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd,
+                            const int32_t* expert_offset, const void* W1, const void* W3,
+                            const void* W2, const void* b1, const void* b2, void* Y, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!xd || !expert_offset || !W1 || !W2 || !Y) return MOE_ERR_INVALID_ARG;
+  if ((cfg->act == MOE_ACT_SWIGLU) != (W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (cfg->act == MOE_ACT_SWIGLU && (b1 || b2)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total_core)) != MOE_OK) return st;
+  return cuda_status(launch_ffn(*cfg, xd, expert_offset, W1, W3, W2, b1, b2, Y,
+                                at<void>(ws, L.ffn_h), max_rows(*cfg),
+                                at<int32_t>(ws, L.hdr), (cudaStream_t)stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* Y, const int32_t* slot_of,
+                         const float* topk_gate, void* y, moe_stream_t stream) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!Y || !slot_of || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(*cfg, Y, slot_of, topk_gate, y, (cudaStream_t)stream));
+}
+
+moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* expert_count,
+                           const float* prob_sum, float* f, float* P, float* L_balance,
+                           int32_t* dropped, moe_stream_t stream) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!expert_count || !prob_sum || !f || !P || !L_balance || !dropped)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_aux(*cfg, expert_count, prob_sum, nullptr, 0, f, P, L_balance,
+                                dropped, (cudaStream_t)stream));
+}
+
+static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
+                                       const moe_layer_inputs_t* in,
+                                       const moe_layer_outputs_t* out, void* y, float* Lout,
+                                       void* ws, cudaStream_t s) {
+  const moe_config_t& c = *cfg;
+  const WsLayout L = ws_layout(c, 0);
+  int32_t* idx = out && out->topk_idx ? out->topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* gate = out && out->topk_gate ? out->topk_gate : at<float>(ws, L.topk_gate);
+  int32_t* slot_of = out && out->slot_of ? out->slot_of : at<int32_t>(ws, L.slot_of);
+  int32_t* count = out && out->expert_count ? out->expert_count : at<int32_t>(ws, L.count);
+  int32_t* offset = out && out->expert_offset ? out->expert_offset : at<int32_t>(ws, L.offset);
+  float* f = out && out->f ? out->f : at<float>(ws, L.f);
+  float* P = out && out->P ? out->P : at<float>(ws, L.P);
+  float* Lb = Lout ? Lout : at<float>(ws, L.L);
+  int32_t* dropped = out && out->dropped ? out->dropped : at<int32_t>(ws, L.dropped);
+  float* logits = out ? out->logits : nullptr;
+  const int rgrid = router_grid(c, 0);
+  float* partial = at<float>(ws, L.router_partial);
+  float* prob_sum = at<float>(ws, L.prob_sum);
+  const int64_t R = max_rows(c);
+  cudaError_t e = launch_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, partial,
+                                rgrid, s);
+  if (e == cudaSuccess)
+    e = launch_dispatch(c, idx, x, count, offset, slot_of, at<int32_t>(ws, L.token_of_row),
+                        at<void>(ws, L.xd), at<int32_t>(ws, L.disp_hist),
+                        at<int32_t>(ws, L.disp_base), R, s);
+  if (e == cudaSuccess)
+    e = launch_ffn(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
+                   at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s);
+  if (e == cudaSuccess) e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s);
+  if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
+  if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
+  return cuda_status(e);
+}
+
+static moe_status_t check_layer_inputs(const moe_config_t* cfg, const moe_layer_inputs_t* in) {
+  if (!in || !in->Wg || !in->W1 || !in->W2) return MOE_ERR_INVALID_ARG;
+  if ((cfg->act == MOE_ACT_SWIGLU) != (in->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (cfg->act == MOE_ACT_SWIGLU && (in->b1 || in->b2)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                               const moe_layer_outputs_t* out, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if (!in->x || !out || !out->y) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg, 0).total_layer)) != MOE_OK) return st;
+  return layer_forward_impl(cfg, in->x, in, out, out->y, out->L_balance, ws,
+                            (cudaStream_t)stream);
+}
+
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
+                                    const moe_layer_inputs_t* in, void* y_host,
+                                    float* L_balance_host, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total_host)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)cfg->T * cfg->d * elem_bytes(*cfg);
+  void* xs = at<void>(ws, L.x_stage);
+  void* ys = at<void>(ws, L.y_stage);
+  if (cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = layer_forward_impl(cfg, xs, in, nullptr, ys, nullptr, ws, s);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (L_balance_host &&
+      cudaMemcpyAsync(L_balance_host, at<float>(ws, L.L), sizeof(float),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

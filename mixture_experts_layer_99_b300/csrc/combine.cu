@@ -1,0 +1,147 @@
+// Gate-weighted combine and load-balance statistics.
+//
+// Combine: y_t = sum_{j: slot_of[t,j] >= 0} g[t,j] Y[slot_of[t,j]], summed in
+// fp32 in slot order j = 0..k-1 (deterministic: each token is produced by one
+// warp, no atomics); y_t = 0 when every slot of t was dropped. This is the
+// output y = sum_{i in K(x)} g_i(x) E_i(x) of the kwkr.cn MoE article, section
+// 2.1, with the masking of dropped tokens from section 2.3.
+//
+// Statistics (section 2.2 of the same article): f_i = count_i/(kT),
+// P_i = (1/T) sum_t p[t,i], L_balance = E sum_i f_i P_i, and the number of
+// dropped slots (the drop-rate diagnostic of section 6.2).
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int NT = 256, NW = NT / 32;
+
+__device__ __forceinline__ void unpack(const uint4& u, float (&f)[8], __nv_bfloat16*) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void unpack(const uint4& u, float (&f)[8], float*) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], __nv_bfloat16*) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+__device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y,
+                                                     const int32_t* __restrict__ slot_of,
+                                                     const float* __restrict__ gate, int T_,
+                                                     int k, int nvec, uint4* __restrict__ y) {
+  constexpr int V = 16 / sizeof(T);
+  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
+  if (t >= T_) return;
+  const int lane = threadIdx.x & 31;
+  int sl[kMaxK];
+  float g[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
+    g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
+  }
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (sl[j] < 0) continue;
+      float f[8];
+      unpack(__ldg(Y + (size_t)sl[j] * nvec + v), f, (T*)nullptr);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], f[i], acc[i]);
+    }
+    y[(size_t)t * nvec + v] = pack(acc, (T*)nullptr);
+  }
+}
+
+// One block. prob_sum is used if given, else the router's per-block partials
+// are reduced here in a fixed order.
+__global__ void __launch_bounds__(NT) aux_kernel(const int32_t* __restrict__ count,
+                                                 const float* __restrict__ prob_sum,
+                                                 const float* __restrict__ partial, int nparts,
+                                                 int T_, int E, int k, int C,
+                                                 float* __restrict__ f, float* __restrict__ P,
+                                                 float* __restrict__ L,
+                                                 int32_t* __restrict__ dropped) {
+  __shared__ double sfp[NT];
+  __shared__ long long skept[NT];
+  double fp = 0.0;
+  long long kept = 0;
+  for (int e = threadIdx.x; e < E; e += NT) {
+    double ps;
+    if (prob_sum) {
+      ps = (double)prob_sum[e];
+    } else {
+      ps = 0.0;
+      for (int b = 0; b < nparts; ++b) ps += (double)partial[(size_t)b * E + e];
+    }
+    const int ce = count[e];
+    const double fe = (double)ce / ((double)k * (double)T_);
+    const double Pe = ps / (double)T_;
+    if (f) f[e] = (float)fe;
+    if (P) P[e] = (float)Pe;
+    fp += fe * Pe;
+    kept += ce < C ? ce : C;
+  }
+  sfp[threadIdx.x] = fp;
+  skept[threadIdx.x] = kept;
+  __syncthreads();
+  for (int w = NT / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      sfp[threadIdx.x] += sfp[threadIdx.x + w];
+      skept[threadIdx.x] += skept[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (L) L[0] = (float)((double)E * sfp[0]);
+    if (dropped) dropped[0] = (int32_t)((long long)k * T_ - skept[0]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
+                           const float* gate, void* y, cudaStream_t s) {
+  const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
+  const unsigned grid = (unsigned)((c.T + NW - 1) / NW);
+  if (c.dtype == MOE_F32)
+    combine_kernel<float><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of, gate,
+                                              c.T, c.k, nvec, static_cast<uint4*>(y));
+  else
+    combine_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of,
+                                                      gate, c.T, c.k, nvec,
+                                                      static_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,
+                       const float* partial, int nparts, float* f, float* P, float* L,
+                       int32_t* dropped, cudaStream_t s) {
+  aux_kernel<<<1, NT, 0, s>>>(count, prob_sum, partial, nparts, c.T, c.E, c.k, c.capacity, f,
+                              P, L, dropped);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

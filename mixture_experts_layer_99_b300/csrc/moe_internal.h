@@ -1,0 +1,93 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 8;
+
+// Router: tokens per tile of the fused router kernel.
+constexpr int kRouterTile = 32;
+// Dispatch: slots per block of the count / assign kernels.
+constexpr int kDispSlotsPerBlock = 1024;
+
+// Device status header at the start of every workspace (int32 words).
+enum HeaderWord : int {
+  kHdrStatus = 0,   // 0 or a moe_status_t recorded by a kernel
+  kHdrWhere = 1,    // which wait gave up
+  kHdrBytes = 256,
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline size_t elem_bytes(const moe_config_t& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+
+// Upper bound on packed rows: every kept slot is one row; sum_e min(count_e, C)
+// <= min(T k, E C).
+inline int64_t max_rows(const moe_config_t& c) {
+  int64_t a = (int64_t)c.T * c.k, b = (int64_t)c.E * c.capacity;
+  return a < b ? a : b;
+}
+
+// Router grid: a fixed bound (4 blocks on each of 148 SMs), independent of the
+// device, so the per-block probability partials (and their fixed-order sum)
+// are the same on every device.
+constexpr int kRouterMaxBlocks = 592;
+inline int router_grid(const moe_config_t& c, int /*unused*/) {
+  int tiles = (c.T + kRouterTile - 1) / kRouterTile;
+  return tiles < kRouterMaxBlocks ? tiles : kRouterMaxBlocks;
+}
+
+inline int disp_blocks(const moe_config_t& c) {
+  int64_t s = (int64_t)c.T * c.k;
+  return (int)((s + kDispSlotsPerBlock - 1) / kDispSlotsPerBlock);
+}
+
+// Workspace regions (byte offsets, 256-aligned). Computed identically by the
+// size query and by every call.
+struct WsLayout {
+  size_t hdr, router_partial, disp_hist, disp_base, ffn_h, ffn_sched;
+  // fused layer intermediates
+  size_t logits, topk_idx, topk_gate, slot_of, count, offset, token_of_row, xd, Y,
+      prob_sum, f, P, L, dropped;
+  // host-io staging
+  size_t x_stage, y_stage;
+  size_t total_core, total_layer, total_host;
+};
+
+WsLayout ws_layout(const moe_config_t& c, int num_sms);
+int device_sm_count();
+
+// ---- launchers (return cudaError_t of the launch) ----
+cudaError_t launch_router(const moe_config_t& c, const void* x, const void* Wg,
+                          const float* bias, const float* noise, float* logits,
+                          int32_t* idx, float* gate, float* partial, int grid,
+                          cudaStream_t s);
+cudaError_t launch_prob_reduce(const moe_config_t& c, const float* partial, int nparts,
+                               float* prob_sum, cudaStream_t s);
+cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,
+                            int32_t* count, int32_t* offset, int32_t* slot_of,
+                            int32_t* token_of_row, void* xd, int32_t* hist, int32_t* base,
+                            int64_t rows_bound, cudaStream_t s);
+cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
+                       const void* W1, const void* W3, const void* W2, const void* b1,
+                       const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
+                       cudaStream_t s);
+cudaError_t launch_ffn_simt(const moe_config_t& c, const void* xd, const int32_t* offset,
+                            const void* W1, const void* W3, const void* W2, const void* b1,
+                            const void* b2, void* Y, void* h, int64_t rows_bound,
+                            cudaStream_t s);
+cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
+                           const float* gate, void* y, cudaStream_t s);
+cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,
+                       const float* partial, int nparts, float* f, float* P, float* L,
+                       int32_t* dropped, cudaStream_t s);
+
+}  // namespace moe

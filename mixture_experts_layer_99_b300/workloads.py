@@ -137,3 +137,31 @@ def small(w: Workload, T: int, d: int, H: int, E: Optional[int] = None,
     return w.with_(T=T, d=d, H=H, E=E if E is not None else w.E,
                    k=k if k is not None else w.k, c=c if c is not None else w.c,
                    name=f"{w.name}[T{T},d{d},H{H}]")
+
+
+def make_routing(T: int, E: int, k: int, seed: int = 0, skew: float = 0.0):
+    """Random top-k expert ids [T, k] int32 (distinct per token) for tests of
+    the stages after the router. ``skew`` > 0 tilts the choice towards low
+    expert ids (ids are the k largest of u + skew * (E - i) / E, u uniform)."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    keys = torch.rand(T, E, generator=gen, dtype=torch.float64)
+    if skew:
+        keys = keys + skew * (E - torch.arange(E, dtype=torch.float64)) / E
+    ids = torch.argsort(keys, dim=1, descending=True, stable=True)[:, :k]
+    return ids.to(torch.int32).contiguous()
+
+
+def make_gates(T: int, k: int, seed: int = 0):
+    """Random positive gates [T, k] fp32 (rows need not sum to 1)."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.rand(T, k, generator=gen, dtype=torch.float32).add_(0.05)
+
+
+def make_rows(R: int, d: int, dtype, seed: int = 0):
+    """Random rows [R, d] of ``dtype`` (N(0,1))."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(R, d, generator=gen, dtype=torch.float32).to(dtype)
+
+
+def to_device(inp: dict, device) -> dict:
+    return {k: (None if v is None else v.to(device).contiguous()) for k, v in inp.items()}

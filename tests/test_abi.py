@@ -1,0 +1,123 @@
+"""CPU checks of the C-ABI library: it loads, exports every call that
+include/moe.h declares, computes the capacity closed form, and rejects bad
+arguments on the host before touching a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+from fractions import Fraction
+
+import pytest
+
+from mixture_experts_layer_99_b300 import moe
+from oracle import moe_oracle as ORC
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    syms = set()
+    for name in os.listdir(os.path.join(ROOT, "include")):
+        if name.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", name)).read()
+            syms |= set(re.findall(r"MOE_API[^;(]*?\b(moe_\w+)\s*\(", text))
+    return syms
+
+
+def test_library_exports_every_declared_symbol():
+    L = moe.lib()
+    syms = declared_symbols()
+    assert "moe_layer_forward" in syms and len(syms) >= 14
+    for s in sorted(syms):
+        assert hasattr(L, s), s
+    assert set(moe.EXPORTED) <= syms
+
+
+def test_abi_version_and_status_strings():
+    L = moe.lib()
+    assert L.moe_abi_version() >= 100
+    for code in range(6):
+        assert L.moe_status_string(code)
+    assert L.moe_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("c,k,T,E", [(Fraction(5, 4), 2, 256, 4), (1, 1, 8192, 8),
+                                     (4, 2, 16384, 8), (2, 2, 32768, 64), (32, 2, 64, 64),
+                                     (Fraction(7, 3), 3, 1001, 17), (Fraction(1, 9), 1, 5, 3)])
+def test_capacity_matches_oracle(c, k, T, E):
+    assert moe.capacity(c, k, T, E) == ORC.capacity(c, k, T, E)
+
+
+def test_capacity_rejects_bad_args():
+    L = moe.lib()
+    assert L.moe_capacity(0, 1, 1, 1, 1) == -1
+    assert L.moe_capacity(1, 1, 1, 1, 0) == -1
+    assert L.moe_capacity(1 << 40, 1, 8, 1 << 20, 1) == -1
+
+
+def _cfg(**kw):
+    base = dict(T=64, d=64, E=4, k=2, H=128, capacity_=40, dtype="bf16", act="gelu", tau=1.0)
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(T=0), dict(E=0), dict(k=0), dict(k=5), dict(d=60),
+                                 dict(H=100), dict(capacity_=0), dict(tau=0.0),
+                                 dict(tau=float("nan")), dict(d=63, dtype="f32")])
+def test_invalid_config_rejected(bad):
+    with pytest.raises(moe.MoEError) as ei:
+        moe.workspace_size(_cfg(**bad))
+    assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("bad", [dict(E=300, k=2), dict(E=16, k=9)])
+def test_unsupported_config(bad):
+    with pytest.raises(moe.MoEError) as ei:
+        moe.workspace_size(_cfg(**bad))
+    assert ei.value.status == 2
+
+
+def test_workspace_size_grows_with_shape():
+    a = moe.workspace_size(_cfg())
+    b = moe.workspace_size(_cfg(T=128))
+    assert 0 < a < b
+    assert moe.workspace_size(_cfg(), host_io=True) > a
+
+
+def test_null_pointers_rejected_before_any_launch():
+    L = moe.lib()
+    cfg = _cfg()
+    r = ctypes.byref(cfg)
+    fake = ctypes.c_void_p(4096)
+    # required pointers missing -> invalid argument, nothing enqueued
+    assert L.moe_router_topk(r, None, fake, None, None, None, fake, fake, fake, fake, 1 << 30,
+                             None) == 1
+    assert L.moe_dispatch(r, fake, fake, None, fake, fake, fake, fake, fake, 1 << 30, None) == 1
+    assert L.moe_combine(r, fake, None, fake, fake, None) == 1
+    assert L.moe_aux_stats(r, fake, fake, fake, fake, None, fake, None) == 1
+    # SwiGLU without W3, GELU with W3
+    sw = _cfg(act="swiglu")
+    assert L.moe_expert_ffn(ctypes.byref(sw), fake, fake, fake, None, fake, None, None, fake,
+                            fake, 1 << 30, None) == 1
+    assert L.moe_expert_ffn(r, fake, fake, fake, fake, fake, None, None, fake, fake, 1 << 30,
+                            None) == 1
+    inp = moe.LayerInputs(None, 4096, None, None, 4096, None, 4096, None, None)
+    out = moe.LayerOutputs(*([4096] + [None] * 10))
+    assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), fake, 1 << 30,
+                               None) == 1
+
+
+def test_workspace_checks():
+    L = moe.lib()
+    cfg = _cfg()
+    r = ctypes.byref(cfg)
+    fake = ctypes.c_void_p(4096)
+    need = moe.workspace_size(cfg)
+    inp = moe.LayerInputs(4096, 4096, None, None, 4096, None, 4096, None, None)
+    out = moe.LayerOutputs(*([4096] + [None] * 10))
+    assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), fake, need - 1,
+                               None) == 3
+    assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), ctypes.c_void_p(4100),
+                               need, None) == 3
+    assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), None, need, None) == 3
+    assert L.moe_router_topk(r, fake, fake, None, None, None, fake, fake, fake, fake, 16,
+                             None) == 3

@@ -1,0 +1,94 @@
+"""End-to-end parity of moe_layer_forward (the fused C-ABI call) against the
+CPU oracle on the five workloads: small variants checked on every token,
+and the full-size shapes checked with routing on every token and the expert
+outputs on a seeded sample (plus every token of the least-loaded experts)."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_99_b300 import moe, workloads as W
+from oracle import moe_oracle as ORC
+from parity_util import TOL_Y, check_layer, np_of, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+WL = W.WORKLOADS
+
+SMALL = {
+    "ref_fp32": WL["ref_fp32"],
+    "switch_small": W.small(WL["switch_top1"], T=1500, d=256, H=512),
+    "mixtral_small": W.small(WL["mixtral"], T=700, d=256, H=384),
+    "longtail_small": W.small(WL["longtail"], T=2000, d=128, H=192),
+    "decode_small": W.small(WL["decode"], T=64, d=512, H=256),
+    "drops_heavy": W.small(WL["longtail"], T=999, d=64, H=64, c=Fraction(1, 3)),
+    "single_expert": W.small(WL["switch_top1"], T=77, d=64, H=128, E=1, k=1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_layer_small(name):
+    res = check_layer(SMALL[name], DEV)
+    assert res["tokens_checked"] == SMALL[name].T
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_layer_seeds(seed):
+    check_layer(W.small(WL["longtail"], T=1024, d=128, H=128), DEV, seed=seed)
+
+
+FULL = {"ref_fp32": None, "switch_top1": 2048, "decode": None, "longtail": 1024,
+        "mixtral": 128}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_layer_full_size(name):
+    res = check_layer(WL[name], DEV, n_sample=FULL[name])
+    print(name, {k: v for k, v in res.items() if k not in ("out", "r")})
+
+
+def test_layer_host_io_matches_device_call():
+    w = W.small(WL["switch_top1"], T=512, d=128, H=256)
+    cfg = moe.config_from_workload(w)
+    inp = W.make_inputs(w)
+    dinp = W.to_device(inp, DEV)
+    out = moe.layer_forward(cfg, dinp)
+    ws = moe.workspace(cfg, DEV, host_io=True)
+    xh = inp["x"].pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    Lh = torch.empty(1, dtype=torch.float32).pin_memory()
+    moe.layer_forward_host(cfg, xh, dinp, yh, ws=ws, L_host=Lh)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, out["y"].cpu())
+    assert Lh.item() == out["L_balance"].item()
+
+
+def test_layer_deterministic():
+    w = W.small(WL["longtail"], T=3000, d=128, H=128)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(W.make_inputs(w), DEV)
+    a = moe.layer_forward(cfg, dinp)
+    b = moe.layer_forward(cfg, dinp)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_layer_zero_router_closed_form():
+    """W_g = 0: every token picks experts 0..k-1 with gates 1/k; tokens at or
+    beyond C lose every slot and get y = 0; L_balance = 1."""
+    w = W.small(WL["mixtral"], T=600, d=64, H=64, E=4, k=2, c=Fraction(1, 2))
+    inp = W.make_inputs(w)
+    inp["Wg"] = torch.zeros_like(inp["Wg"])
+    cfg = moe.config_from_workload(w)
+    C = cfg.capacity          # ceil(0.5 * 2 * 600 / 4) = 150
+    assert C == 150
+    out = moe.layer_forward(cfg, W.to_device(inp, DEV))
+    torch.cuda.synchronize()
+    assert (out["topk_idx"].cpu() == torch.tensor([0, 1], dtype=torch.int32)).all()
+    assert (out["y"][C:] == 0).all()
+    assert abs(out["L_balance"].item() - 1.0) < 1e-6
+    assert out["dropped"].item() == 2 * (600 - C)
+    r = ORC.moe_forward(inp, k=2, c=w.c, act=w.act, tokens=np.arange(C))
+    assert rel_err(np_of(out["y"][:C]), r["y"]) <= TOL_Y["bf16"]

@@ -488,3 +488,21 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
         except Exception:   # an assertion, or a shape error from a wrong operand
             failed.append(pin.__name__)
     assert failed, f"planted mistake {name} passed every pin"
+
+
+def test_combine_rows_and_balance_helpers():
+    """The stage-level helpers agree with the layer-level functions."""
+    rng = _rng(11)
+    T, E, k, d = 30, 5, 2, 4
+    l = rng.standard_normal((T, E))
+    r = ORC.route_from_logits(l, k, 10)
+    Yrows = rng.standard_normal((int(r["offset"][-1]), d))
+    y = ORC.combine_rows(Yrows, r["slot_of"], r["gates"])
+    for t in range(T):
+        want = np.zeros(d)
+        for j in range(k):
+            if r["slot_of"][t, j] >= 0:
+                want += r["gates"][t, j] * Yrows[r["slot_of"][t, j]]
+        np.testing.assert_allclose(y[t], want, rtol=0, atol=1e-14)
+    b = ORC.balance_from_sums(r["count"], r["p"].sum(axis=0), T, k, r["kept"])
+    assert abs(b["L"] - r["L"]) < 1e-15 and b["dropped"] == r["dropped"]
