@@ -230,12 +230,33 @@ def aux_stats(p, count, kept, k: int):
     """f_i = count_i / (k T) (before drops), P_i = (1/T) sum_t p[t,i],
     L_balance = E * sum_i f_i P_i, dropped = k T - sum_i kept_i."""
     p = np.asarray(p, dtype=np.float64)
-    T, E = p.shape
+    T = p.shape[0]
+    return balance_from_sums(count, p.sum(axis=0), T, k, kept)
+
+
+def balance_from_sums(count, prob_sum, T: int, k: int, kept):
+    """The same statistics from per-expert sums: f_i = count_i / (k T),
+    P_i = prob_sum_i / T, L_balance = E sum_i f_i P_i, dropped = kT - sum kept."""
     f = np.asarray(count, dtype=np.float64) / float(k * T)
-    P = p.sum(axis=0) / float(T)
+    P = np.asarray(prob_sum, dtype=np.float64) / float(T)
+    E = f.shape[0]
     L = float(E) * float((f * P).sum())
-    dropped = int(k * T - int(np.asarray(kept).sum()))
+    dropped = int(k * T - int(np.asarray(kept, dtype=np.int64).sum()))
     return dict(f=f, P=P, L=L, dropped=dropped)
+
+
+def combine_rows(Yrows, slot_of, gates):
+    """Combine step alone: y_t = sum over j with slot_of[t,j] >= 0 of
+    g[t,j] * Yrows[slot_of[t,j]] (fp64), y_t = 0 if no slot was kept."""
+    Yrows = as_f64(Yrows)
+    slot_of = np.asarray(slot_of)
+    gates = np.asarray(gates, dtype=np.float64)
+    T, k = slot_of.shape
+    y = np.zeros((T, Yrows.shape[1]), dtype=np.float64)
+    for j in range(k):
+        keep = slot_of[:, j] >= 0
+        y[keep] += gates[keep, j][:, None] * Yrows[slot_of[keep, j]]
+    return y
 
 
 # --------------------------------------------------------------------------
