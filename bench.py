@@ -1,0 +1,430 @@
+"""Benchmark of the MoE layer forward on B300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-cpu-baseline]
+
+A step is one moe_layer_forward (router, dispatch, grouped expert FFN,
+combine, statistics) over one batch of the workload, inputs resident in HBM.
+Steps rotate over several input + weight sets whose total exceeds the L2
+cache, so no step reads the previous step's data from L2.
+
+Under torchrun (N > 1) every rank runs its own independent batch (the layer
+is token-parallel; nothing is exchanged on the data path), the K steps are
+bracketed by a barrier and a device synchronisation, the time is the maximum
+over ranks and ``value`` is the total tokens of all ranks per second.
+
+``--impl reference`` times the CPU oracle instead (rank 0 only), each step a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_layer_99_b300 import workloads as W  # noqa: E402
+
+METRIC = ("MoE-layer fwd tokens/s at 1 B300; expert-GEMM TFLOP/s % of BF16 peak; "
+          "router/dispatch GB/s")
+UNIT = "tokens/s"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"])
+        # samples are ~100 ms apart; keep those after the warm-up began
+        reasons = set()
+        for r in rows:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        loaded = [r["sm"] for r in rows if r["sm"] > 0]
+        return dict(sm_mhz=statistics.median(loaded) if loaded else None,
+                    sm_max_mhz=max(r["smax"] for r in rows), reasons=sorted(reasons),
+                    samples=len(rows))
+
+
+# ---------------------------------------------------------------- work model
+def algorithmic(w, kept: int, n_active: int):
+    """Algorithmic FLOPs and bytes of one layer call (what the method must
+    compute or move), per part."""
+    s = w.elem_bytes
+    T, d, E, k, H = w.T, w.d, w.E, w.k, w.H
+    nm = w.nmat
+    router_b = T * d * s + E * d * s + (T * E * 4 if w.noise else 0) + T * k * 8 + E * 4
+    router_f = 2 * T * d * E
+    disp_b = T * k * 4 * 2 + 2 * kept * d * s + 8 * E
+    gemm_f = kept * 2 * nm * d * H
+    gemm_b = n_active * nm * d * H * s + 2 * kept * d * s
+    comb_b = kept * d * s + T * k * 8 + T * d * s
+    return dict(router_bytes=router_b, router_flops=router_f, dispatch_bytes=disp_b,
+                gemm_flops=gemm_f, gemm_bytes=gemm_b, combine_bytes=comb_b)
+
+
+def footprint_bytes(inp):
+    return sum(v.numel() * v.element_size() for v in inp.values() if v is not None)
+
+
+def traffic_record(kernel_src_sha):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != kernel_src_sha:
+        return None
+    return rec
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_99_b300", "csrc")
+    for name in ("ffn_tc.cu", "tc_ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------- CPU oracle
+def time_oracle(w, target_s=12.0, seed=0):
+    """Times the oracle (fp64 numpy, all host cores its BLAS uses) on the
+    first n tokens of the workload's batch taken as a batch of their own."""
+    from oracle import moe_oracle as ORC
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:  # pragma: no cover
+        cores = os.cpu_count()
+    inp = W.make_inputs(w)
+
+    def run(n):
+        sub = dict(inp)
+        sub["x"] = inp["x"][:n]
+        if inp.get("noise") is not None:
+            sub["noise"] = inp["noise"][:n]
+        t0 = time.perf_counter()
+        ORC.moe_forward(sub, k=w.k, c=w.c, act=w.act, tau=w.tau)
+        return time.perf_counter() - t0
+
+    n = min(w.T, 64)
+    t = run(n)
+    while t < target_s / 4 and n < w.T:
+        n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3) / 2)))
+        t = run(n)
+    return dict(value=n / t, unit=UNIT, cores=cores, kind="oracle",
+                sample=(f"first {n} of {w.T} tokens of the seed-{w.seed} {w.name} batch as a "
+                        f"batch of their own (capacity recomputed): full fp64 numpy forward "
+                        f"(router, top-k, dispatch, experts, combine, statistics) in {t:.2f} s"),
+                seconds=t, tokens=n)
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    per_step = time_oracle(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = per_step["tokens"]
+    from oracle import moe_oracle as ORC
+    inp = W.make_inputs(w)
+    sub = dict(inp)
+    sub["x"] = inp["x"][:n]
+    if inp.get("noise") is not None:
+        sub["noise"] = inp["noise"][:n]
+    for _ in range(args.warmup):
+        ORC.moe_forward(sub, k=w.k, c=w.c, act=w.act, tau=w.tau)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ORC.moe_forward(sub, k=w.k, c=w.c, act=w.act, tau=w.tau)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=dt * 1e3, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                impl="reference",
+                config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
+                            sample_tokens=n),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=per_step["cores"],
+                                  kind="oracle", sample=per_step["sample"]),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="switch_top1", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    from mixture_experts_layer_99_b300 import moe
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    peaks = load_peaks()
+
+    # ---- inputs: rotating sets, different seed per rank and per set
+    base = W.make_inputs(w, seed=w.seed + 1000 * rank)
+    fp = footprint_bytes(base)
+    nsets = max(2, math.ceil(3 * L2_BYTES / fp))
+    sets = [W.to_device(base, dev)]
+    for i in range(1, nsets):
+        sets.append(W.to_device(W.make_inputs(w, seed=w.seed + 1000 * rank + i), dev))
+    cfg = moe.config_from_workload(w)
+    ws = moe.workspace(cfg, dev, host_io=True)
+    out = moe.alloc_outputs(cfg, dev, full=True)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- routing statistics of set 0 (for the algorithmic work model)
+    moe.layer_forward(cfg, sets[0], ws=ws, out=out)
+    torch.cuda.synchronize(dev)
+    offs = out["expert_offset"].cpu().numpy()
+    kept = int(offs[-1])
+    n_active = int((np.diff(offs) > 0).sum())
+    work = algorithmic(w, kept, n_active)
+
+    def step(i):
+        moe.layer_forward(cfg, sets[i % nsets], ws=ws, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clk = clocks.stop() if clocks else None
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = w.T * world / (ms / 1e3)
+    status = moe.device_status(ws)
+
+    # ---- per-stage timing (same rotation; each stage alone, events on this stream)
+    st = {}
+    reps = max(20, min(args.steps, 200))
+    dinp = sets
+    lg, idx, gate, psum = (out["logits"], out["topk_idx"], out["topk_gate"],
+                           torch.empty(cfg.E, dtype=torch.float32, device=dev))
+    rows = min(cfg.T * cfg.k, cfg.E * cfg.capacity)
+    xd = torch.empty(cfg.T * cfg.k, cfg.d, dtype=sets[0]["x"].dtype, device=dev)
+    Yb = torch.empty_like(xd)
+    disp = moe.dispatch(cfg, idx, sets[0]["x"], ws=ws)
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    st["router"] = timed(lambda i: moe._call(
+        "moe_router_topk", moe.ctypes.byref(cfg), dinp[i % nsets]["x"].data_ptr(),
+        dinp[i % nsets]["Wg"].data_ptr(), moe._ptr(dinp[i % nsets]["bias"]),
+        moe._ptr(dinp[i % nsets]["noise"]), lg.data_ptr(), idx.data_ptr(), gate.data_ptr(),
+        psum.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream))
+    st["dispatch"] = timed(lambda i: moe._call(
+        "moe_dispatch", moe.ctypes.byref(cfg), idx.data_ptr(), dinp[i % nsets]["x"].data_ptr(),
+        disp["count"].data_ptr(), disp["offset"].data_ptr(), disp["slot_of"].data_ptr(),
+        disp["token_of_row"].data_ptr(), xd.data_ptr(), ws.data_ptr(), ws.numel(),
+        stream.cuda_stream))
+    st["expert_ffn"] = timed(lambda i: moe._call(
+        "moe_expert_ffn", moe.ctypes.byref(cfg), xd.data_ptr(), disp["offset"].data_ptr(),
+        dinp[i % nsets]["W1"].data_ptr(), moe._ptr(dinp[i % nsets]["W3"]),
+        dinp[i % nsets]["W2"].data_ptr(), moe._ptr(dinp[i % nsets]["b1"]),
+        moe._ptr(dinp[i % nsets]["b2"]), Yb.data_ptr(), ws.data_ptr(), ws.numel(),
+        stream.cuda_stream))
+    st["combine"] = timed(lambda i: moe._call(
+        "moe_combine", moe.ctypes.byref(cfg), Yb.data_ptr(), disp["slot_of"].data_ptr(),
+        gate.data_ptr(), out["y"].data_ptr(), stream.cuda_stream))
+    st["aux_stats"] = timed(lambda i: moe._call(
+        "moe_aux_stats", moe.ctypes.byref(cfg), disp["count"].data_ptr(), psum.data_ptr(),
+        out["f"].data_ptr(), out["P"].data_ptr(), out["L_balance"].data_ptr(),
+        out["dropped"].data_ptr(), stream.cuda_stream))
+
+    # ---- end to end through the host-buffer C call (pinned host x and y)
+    xh = [s["x"].cpu().pin_memory() for s in sets[:2]]
+    yh = torch.empty_like(xh[0]).pin_memory()
+    Lh = torch.empty(1, dtype=torch.float32).pin_memory()
+    e2e_steps = max(10, min(args.steps, 500))
+    for i in range(3):
+        moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh, ws=ws, L_host=Lh)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(e2e_steps):
+        moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh, ws=ws, L_host=Lh)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    bytes_x = cfg.T * cfg.d * sets[0]["x"].element_size()
+
+    # ---- roofline of the dominant kernel (the grouped GEMM, two launches per call)
+    gemm_ms = st["expert_ffn"]
+    achieved = work["gemm_flops"] / (gemm_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    rec = traffic_record(source_sha())
+    roof = dict(kernel="grouped_gemm_tc_kernel (GEMM1 + GEMM2 launches)", bound="tensor",
+                achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
+                peak_source=f"{peaks['source']} burst bf16",
+                traffic=None if rec is None else rec["bytes_per_launch"],
+                algorithmic_flops_per_launch=work["gemm_flops"] / 2,
+                launch_ms=gemm_ms / 2)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = time_oracle(w)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        hbm = peaks["hbm_gbs"]
+        line = dict(
+            metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+            vs_baseline=None, dtype="bf16" if w.dtype == "bf16" else "f32",
+            data="synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+            config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
+                        capacity=cfg.capacity, kept_rows=kept, active_experts=n_active,
+                        parallelism=f"replicas x{world}",
+                        l2=f"{nsets} rotating input+weight sets of {fp / 2**20:.0f} MiB "
+                           f"(> L2 between reuses)"),
+            roofline=roof,
+            cpu_baseline=cpu,
+            e2e=dict(value=w.T * world / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=bytes_x,
+                     d2h_bytes_per_step=bytes_x + 4),
+            gpu_launches=moe.lib().moe_layer_forward_launch_count(moe.ctypes.byref(cfg))
+            * args.steps,
+            clocks=clk,
+            stages_ms=st,
+            stages_roofline=dict(
+                router_gbs=work["router_bytes"] / (st["router"] / 1e3) / 1e9,
+                router_hbm_frac=work["router_bytes"] / (st["router"] / 1e3) / 1e9 / hbm,
+                dispatch_gbs=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9,
+                dispatch_hbm_frac=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9 / hbm,
+                combine_gbs=work["combine_bytes"] / (st["combine"] / 1e3) / 1e9,
+                combine_hbm_frac=work["combine_bytes"] / (st["combine"] / 1e3) / 1e9 / hbm,
+                gemm_tflops=achieved, gemm_frac_burst=achieved / peak,
+                gemm_weight_gbs=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9,
+                hbm_peak_gbs=hbm),
+            device_status=status[0],
+        )
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

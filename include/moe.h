@@ -210,6 +210,10 @@ MOE_API moe_status_t moe_layer_forward(const moe_config_t *cfg, const moe_layer_
                                const moe_layer_outputs_t *out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* Number of kernels one moe_layer_forward call launches for this shape
+ * (0 if cfg is invalid). Host only. */
+MOE_API int32_t moe_layer_forward_launch_count(const moe_config_t *cfg);
+
 /* As moe_layer_forward, but x_host [T, d] and y_host [T, d] are HOST buffers
  * (page-locked for asynchronous copies); the weights in `in` stay on the device
  * (in->x is ignored). The copies in and out run on `stream` inside the call's

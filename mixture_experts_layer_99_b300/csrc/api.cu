@@ -60,7 +60,8 @@ cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* off
                        const void* W1, const void* W3, const void* W2, const void* b1,
                        const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
                        cudaStream_t s) {
-  (void)hdr;
+  if (c.dtype == MOE_BF16)
+    return launch_ffn_tc(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, hdr, s);
   return launch_ffn_simt(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, s);
 }
 
@@ -284,6 +285,13 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const moe_layer_inputs_t
   if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg, 0).total_layer)) != MOE_OK) return st;
   return layer_forward_impl(cfg, in->x, in, out, out->y, out->L_balance, ws,
                             (cudaStream_t)stream);
+}
+
+int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  // router, dispatch (count, scan, assign, gather), GEMM1, GEMM2, combine,
+  // probability reduction, statistics
+  return 10;
 }
 
 moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,

@@ -1,0 +1,429 @@
+// Grouped expert FFN on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA. bf16 in, fp32 accumulation in TMEM.
+//
+// The expert FFN of the kwkr.cn MoE article ("MoE sparse activation: from
+// the math to the code"), section 3.1 (Linear -> GELU -> Linear), with the
+// SwiGLU form W2 (silu(W1 x) * (W3 x)) for the 4096 -> 14336 experts of the
+// lpnh.cn MoE guide, section 3.2. The per-expert loop of the article's
+// section 3.2 becomes one persistent launch per GEMM over all experts'
+// tiles; expert e owns packed rows [offset_e, offset_{e+1}).
+//
+// Kernel layout (one CTA per SM, 320 threads):
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage
+//   warp 1      TMEM owner and MMA issuer (one thread), 128 x 256 x 16 MMAs
+//   warps 2-9   epilogue: TMEM -> registers -> activation -> bf16 -> global
+// Two 256-column fp32 accumulators in TMEM let the epilogue of one tile run
+// under the MMAs of the next. M-tiles never cross an expert boundary: a tile
+// that starts at row offset_e + 128 i loads rows of the next expert (or TMA
+// zero fill past the buffer) and the epilogue masks them out.
+//
+// GEMM1 (GELU):   h[r, n] = gelu(sum_k xd[r,k] W1[e,n,k] + b1[e,n])   tile N = 256
+// GEMM1 (SwiGLU): B tile = 128 rows of W1 then the same 128 rows of W3, so one
+//                 N = 256 MMA yields gate and up: h = silu(gate) * up   tile N = 128
+// GEMM2:          Y[r, n] = sum_k h[r,k] W2[e,n,k] (+ b2[e,n])        tile N = 256
+#include "moe_internal.h"
+#include "tc_ptx.cuh"
+
+#include <math.h>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK = 64;       // one 128-byte swizzle row of bf16
+constexpr int UMMA_N = 256;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_WARPS = 8;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = UMMA_N * BK * 2;      // 32 KB
+constexpr int TMEM_COLS = 2 * UMMA_N;         // two accumulators
+
+enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2 };
+
+struct SmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t final_bar;
+  uint32_t tmem_base;
+  int abort_flag;
+  int n_tiles_total;
+  int off[kMaxE + 1];
+  int tbase[kMaxE + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + sizeof(SmemTail);
+
+__device__ __forceinline__ float gelu_erf(float u) {
+  return 0.5f * u * (1.f + erff(u * 0.70710678118654752f));
+}
+__device__ __forceinline__ float silu_f(float u) { return u / (1.f + expf(-u)); }
+
+struct TileInfo {
+  int e, m0, mend, n0;
+};
+
+// tile -> (expert, first row, end row of the expert, first output column)
+__device__ __forceinline__ TileInfo tile_info(const SmemTail& st, int E, int n_tiles_n, int tile,
+                                              int bn_out) {
+  int lo = 0, hi = E - 1;  // largest e with tbase[e] <= tile
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (st.tbase[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo;
+  const int local = tile - st.tbase[e];
+  const int mt = (st.off[e + 1] - st.off[e] + BM - 1) / BM;
+  TileInfo ti;
+  ti.e = e;
+  ti.m0 = st.off[e] + (local % mt) * BM;
+  ti.mend = st.off[e + 1];
+  ti.n0 = (local / mt) * bn_out;
+  return ti;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmB3,
+                           const int32_t* __restrict__ offset, int E, int N, int K,
+                           const __nv_bfloat16* __restrict__ bias,
+                           __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr) {
+  constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * (A_BYTES + B_BYTES));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // ---- set-up: barriers, TMEM, tile table
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&st.full[s], 1);
+      mbar_init(&st.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&st.tmem_full[a], 1);
+      mbar_init(&st.tmem_empty[a], EPI_WARPS * 32);
+    }
+    mbar_init(&st.final_bar, 1);
+    st.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (MODE == kSwiglu) prefetch_tmap(&tmB3);
+  }
+  if (warp == 1) {
+    tmem_alloc(&st.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  for (int i = tid; i <= E; i += NUM_THREADS) st.off[i] = offset[i];
+  __syncthreads();
+  const int n_tiles_n = (N + BN_OUT - 1) / BN_OUT;
+  if (warp == 2) {  // tbase[e] = sum_{e'<e} m-tiles(e') * n_tiles_n
+    int run = 0;
+    for (int e0 = 0; e0 <= E; e0 += 32) {
+      const int e = e0 + lane;
+      const int mt = e < E ? (st.off[e + 1] - st.off[e] + BM - 1) / BM : 0;
+      int incl = mt * n_tiles_n;
+      const int v = incl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e <= E) st.tbase[e] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) st.n_tiles_total = st.tbase[E];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = st.n_tiles_total;
+  const uint32_t tmem_base = st.tmem_base;
+  const int num_kb = (K + BK - 1) / BK;
+  volatile int* abort_flag = &st.abort_flag;
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = tile_info(st, E, n_tiles_n, tile, BN_OUT);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, hdr, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&st.full[stage], A_BYTES + B_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &st.full[stage], kb * BK, ti.m0);
+          if (MODE == kSwiglu) {
+            tma_load_3d(sB + stage * B_BYTES, &tmB, &st.full[stage], kb * BK, ti.n0, ti.e);
+            tma_load_3d(sB + stage * B_BYTES + B_BYTES / 2, &tmB3, &st.full[stage], kb * BK,
+                        ti.n0, ti.e);
+          } else {
+            tma_load_3d(sB + stage * B_BYTES, &tmB, &st.full[stage], kb * BK, ti.n0, ti.e);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (--s < 0) {
+            s = STAGES - 1;
+            ph ^= 1u;
+          }
+          volatile int no_abort = 0;
+          mbar_wait(&st.full[s], ph, &no_abort, nullptr, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, UMMA_N);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!mbar_wait(&st.tmem_empty[acc], acc_phase ^ 1u, abort_flag, hdr, 2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * UMMA_N);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&st.full[stage], phase, abort_flag, hdr, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(a0 + stage * A_BYTES);
+          const uint64_t bdesc = sdesc_kmajor_sw128(b0 + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advance along K inside the 128-byte swizzle row: 16 bf16 = 32 B
+            umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&st.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&st.tmem_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // wait for the MMAs already issued before TMEM is released
+        umma_commit(&st.final_bar);
+        volatile int no_abort = 0;
+        mbar_wait(&st.final_bar, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else {
+    // ================= epilogue (warps 2..9)
+    const int ew = warp - 2;
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int half = ew >> 2;              // which half of the tile's columns
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = tile_info(st, E, n_tiles_n, tile, BN_OUT);
+      if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 4)) break;
+      tc_fence_after();
+      const int row = ti.m0 + quarter * 32 + lane;
+      const bool row_ok = row < ti.mend;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * UMMA_N);
+      __nv_bfloat16* orow = out + (size_t)row * N;
+      constexpr int CHUNKS = (MODE == kSwiglu ? 64 : 128) / 32;
+#pragma unroll 1
+      for (int ch = 0; ch < CHUNKS; ++ch) {
+        const int c = (MODE == kSwiglu ? 64 : 128) * half + 32 * ch;  // tile-local out column
+        uint32_t r[32];
+        float v[32];
+        if (MODE == kSwiglu) {
+          uint32_t u[32];
+          tmem_ld32(t_row + (uint32_t)c, r);
+          tmem_ld32(t_row + (uint32_t)(128 + c), u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = silu_f(__uint_as_float(r[j])) * __uint_as_float(u[j]);
+        } else {
+          tmem_ld32(t_row + (uint32_t)c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if (bias) {
+            const __nv_bfloat16* be = bias + (size_t)ti.e * N + ti.n0 + c;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (ti.n0 + c + j < N) v[j] += __bfloat162float(be[j]);
+          }
+          if (MODE == kGelu) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+          }
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = ti.n0 + c + 8 * q;
+            if (col + 8 <= N) {
+              uint4 pk;
+              __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                h2[j] = __floats2bfloat162_rn(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
+              *reinterpret_cast<uint4*>(orow + col) = pk;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&st.tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 [rows, K] row-major, box [128 rows, 64 cols], 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {K, rows};
+  cuuint64_t gstride[1] = {K * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 [E, N, K] (K contiguous), box [1, box_rows, 64], 128-byte swizzle.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t E,
+                 uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t gdim[3] = {K, N, E};
+  cuuint64_t gstride[2] = {K * 2, N * K * 2};
+  cuuint32_t box[3] = {BK, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                        const int32_t* offset, int E, int N, int K, const void* bias, void* out,
+                        int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
+  const int64_t tiles_bound = ((rows_bound + BM - 1) / BM + E) * ((N + BN_OUT - 1) / BN_OUT);
+  const int sms = device_sm_count();
+  const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
+  grouped_gemm_tc_kernel<MODE><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
+      a, b, b3, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
+      static_cast<__nv_bfloat16*>(out), hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
+                          const void* W1, const void* W3, const void* W2, const void* b1,
+                          const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
+                          cudaStream_t s) {
+  CUtensorMap mx, mh, mw1, mw3, mw2;
+  const uint64_t R = (uint64_t)rows_bound;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (!make_map_2d(&mx, xd, c.d, R) || !make_map_2d(&mh, h, c.H, R) ||
+      !make_map_3d(&mw1, W1, c.d, c.H, c.E, swiglu ? 128 : UMMA_N) ||
+      !make_map_3d(&mw2, W2, c.H, c.d, c.E, UMMA_N))
+    return cudaErrorInvalidValue;
+  if (swiglu && !make_map_3d(&mw3, W3, c.d, c.H, c.E, 128)) return cudaErrorInvalidValue;
+  if (!swiglu) mw3 = mw1;
+  cudaError_t e;
+  if (swiglu)
+    e = launch_gemm<kSwiglu>(mx, mw1, mw3, offset, c.E, c.H, c.d, nullptr, h, rows_bound, hdr, s);
+  else
+    e = launch_gemm<kGelu>(mx, mw1, mw3, offset, c.E, c.H, c.d, b1, h, rows_bound, hdr, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemm<kPlain>(mh, mw2, mw2, offset, c.E, c.d, c.H, swiglu ? nullptr : b2, Y,
+                             rows_bound, hdr, s);
+}
+
+}  // namespace moe

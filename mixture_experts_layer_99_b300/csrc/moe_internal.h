@@ -84,6 +84,10 @@ cudaError_t launch_ffn_simt(const moe_config_t& c, const void* xd, const int32_t
                             const void* W1, const void* W3, const void* W2, const void* b1,
                             const void* b2, void* Y, void* h, int64_t rows_bound,
                             cudaStream_t s);
+cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
+                          const void* W1, const void* W3, const void* W2, const void* b1,
+                          const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
+                          cudaStream_t s);
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
                            const float* gate, void* y, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,

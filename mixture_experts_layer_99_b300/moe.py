@@ -28,7 +28,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspace_size",
             "moe_workspace_size_host", "moe_workspace_init", "moe_device_status",
             "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-            "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host"]
+            "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
+            "moe_layer_forward_launch_count"]
 
 
 class MoEError(RuntimeError):
@@ -90,6 +91,7 @@ def lib():
         "moe_aux_stats": (c_int32, [cfgp, vp, vp, vp, vp, vp, vp, vp]),
         "moe_layer_forward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs),
                                         vp, c_size_t, vp]),
+        "moe_layer_forward_launch_count": (c_int32, [cfgp]),
         "moe_layer_forward_host": (c_int32, [cfgp, vp, POINTER(LayerInputs), vp, vp, vp,
                                              c_size_t, vp]),
     }
