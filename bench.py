@@ -153,9 +153,8 @@ def traffic_record(kernel_src_sha):
 def source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_layer_99_b300", "csrc")
-    for name in ("ffn_tc.cu", "tc_ptx.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(csrc, "ffn_tc.cu"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()
 
 

@@ -22,7 +22,8 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
     return at;
   };
   L.hdr = take(kHdrBytes);
-  L.router_partial = take(rgrid * E * 4);
+  L.router_partial = take((rgrid > (size_t)kRouterTcMaxBlocks ? rgrid : kRouterTcMaxBlocks) * E * 4);
+  L.router_tile_hist = take((size_t)router_tc_tiles(c) * E * 4);
   L.disp_hist = take(nblk * E * 4);
   L.disp_base = take(nblk * E * 4);
   L.ffn_h = take(R * (size_t)c.H * s);
@@ -54,6 +55,23 @@ int device_sm_count() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
   return n;
+}
+
+// Router: the tensor-core kernel for bf16 with E <= 64, the FMA kernel
+// otherwise (fp32 needs fp32 products; E > 64 exceeds the register row).
+// Returns the number of per-CTA probability partials written.
+cudaError_t run_router(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
+                       const float* noise, float* logits, int32_t* idx, float* gate,
+                       void* ws, const WsLayout& L, int* nparts, cudaStream_t s) {
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.router_partial);
+  if (router_tc_supported(c)) {
+    *nparts = router_tc_grid(c);
+    return launch_router_tc(c, x, Wg, bias, noise, logits, idx, gate, partial,
+                            reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.router_tile_hist),
+                            reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hdr), s);
+  }
+  *nparts = router_grid(c, 0);
+  return launch_router(c, x, Wg, bias, noise, logits, idx, gate, partial, *nparts, s);
 }
 
 cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
@@ -174,11 +192,11 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void*
   const WsLayout L = ws_layout(*cfg, 0);
   if ((st = check_ws(ws, ws_bytes, L.total_core)) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const int grid = router_grid(*cfg, 0);
-  float* partial = at<float>(ws, L.router_partial);
-  cudaError_t e = launch_router(*cfg, x, Wg, bias, noise, logits, topk_idx, topk_gate,
-                                partial, grid, s);
-  if (e == cudaSuccess) e = launch_prob_reduce(*cfg, partial, grid, prob_sum, s);
+  int nparts = 0;
+  cudaError_t e = run_router(*cfg, x, Wg, bias, noise, logits, topk_idx, topk_gate, ws, L,
+                             &nparts, s);
+  if (e == cudaSuccess)
+    e = launch_prob_reduce(*cfg, at<float>(ws, L.router_partial), nparts, prob_sum, s);
   return cuda_status(e);
 }
 
@@ -249,12 +267,12 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
   float* Lb = Lout ? Lout : at<float>(ws, L.L);
   int32_t* dropped = out && out->dropped ? out->dropped : at<int32_t>(ws, L.dropped);
   float* logits = out ? out->logits : nullptr;
-  const int rgrid = router_grid(c, 0);
+  int rgrid = 0;
   float* partial = at<float>(ws, L.router_partial);
   float* prob_sum = at<float>(ws, L.prob_sum);
   const int64_t R = max_rows(c);
-  cudaError_t e = launch_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, partial,
-                                rgrid, s);
+  cudaError_t e = run_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, ws, L,
+                             &rgrid, s);
   if (e == cudaSuccess)
     e = launch_dispatch(c, idx, x, count, offset, slot_of, at<int32_t>(ws, L.token_of_row),
                         at<void>(ws, L.xd), at<int32_t>(ws, L.disp_hist),

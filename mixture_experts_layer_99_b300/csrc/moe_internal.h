@@ -45,6 +45,19 @@ inline int router_grid(const moe_config_t& c, int /*unused*/) {
   return tiles < kRouterMaxBlocks ? tiles : kRouterMaxBlocks;
 }
 
+// Tensor-core router: 128-token tiles, at most one CTA per SM of a 148-SM
+// B300 (a fixed bound, so the per-CTA partial sums do not depend on the
+// device).
+constexpr int kRouterTcTile = 128;
+constexpr int kRouterTcMaxBlocks = 148;
+inline int router_tc_tiles(const moe_config_t& c) {
+  return (c.T + kRouterTcTile - 1) / kRouterTcTile;
+}
+inline int router_tc_grid(const moe_config_t& c) {
+  const int t = router_tc_tiles(c);
+  return t < kRouterTcMaxBlocks ? t : kRouterTcMaxBlocks;
+}
+
 inline int disp_blocks(const moe_config_t& c) {
   int64_t s = (int64_t)c.T * c.k;
   return (int)((s + kDispSlotsPerBlock - 1) / kDispSlotsPerBlock);
@@ -53,7 +66,7 @@ inline int disp_blocks(const moe_config_t& c) {
 // Workspace regions (byte offsets, 256-aligned). Computed identically by the
 // size query and by every call.
 struct WsLayout {
-  size_t hdr, router_partial, disp_hist, disp_base, ffn_h, ffn_sched;
+  size_t hdr, router_partial, router_tile_hist, disp_hist, disp_base, ffn_h, ffn_sched;
   // fused layer intermediates
   size_t logits, topk_idx, topk_gate, slot_of, count, offset, token_of_row, xd, Y,
       prob_sum, f, P, L, dropped;
@@ -70,6 +83,11 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* Wg,
                           const float* bias, const float* noise, float* logits,
                           int32_t* idx, float* gate, float* partial, int grid,
                           cudaStream_t s);
+bool router_tc_supported(const moe_config_t& c);
+cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
+                             const float* bias, const float* noise, float* logits, int32_t* idx,
+                             float* gate, float* partial, int32_t* tile_hist, int32_t* hdr,
+                             cudaStream_t s);
 cudaError_t launch_prob_reduce(const moe_config_t& c, const float* partial, int nparts,
                                float* prob_sum, cudaStream_t s);
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,

@@ -1,0 +1,401 @@
+// Fused router on the tcgen05 tensor cores for bf16 tokens and E <= 64.
+//
+// logits l = (x Wg^T + b + g) / tau, softmax p = softmax(l), the k largest
+// logits (descending, ties to the lower expert index), renormalised gates
+// g_j = p_{K_j} / sum_m p_{K_m}, per-CTA sums of p for P_i and per-tile
+// selection counts for the dispatch. This is the gate of the kwkr.cn MoE
+// article ("MoE sparse activation: from the math to the code"), section 2.1,
+// fused with softmax and top-k as its section 5.3 suggests; bias, noise and
+// temperature as in the lpnh.cn MoE guide, section 3.3.
+//
+// The contraction x Wg^T (E tiny) is HBM-bound: the kernel streams 128-token
+// tiles of x through TMA and issues one 128 x E_pad x 16 MMA per 16-wide K
+// step, so each epilogue thread owns one token's whole logit row in TMEM.
+//   warp 0      TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
+//   warp 1      TMEM owner, MMA issuer
+//   warps 2-5   epilogue: one thread per token
+#include "moe_internal.h"
+#include "tc_ptx.cuh"
+
+#include <math.h>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int NUM_THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;
+
+template <int EP>
+struct RouterCfg {
+  static constexpr int B_BYTES = EP * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
+  static constexpr int TCOLS = 2 * EP <= 32 ? 32 : (2 * EP <= 64 ? 64 : 128);
+};
+
+template <int EP>
+struct RouterSmem {
+  uint64_t full[RouterCfg<EP>::STAGES];
+  uint64_t empty[RouterCfg<EP>::STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t final_bar;
+  uint32_t tmem_base;
+  int abort_flag;
+  float red[4][EP];
+  float part[EP];
+  int hist[EP];
+};
+
+template <int EP>
+constexpr size_t router_smem_bytes() {
+  return 1024 + RouterCfg<EP>::STAGES * RouterCfg<EP>::STAGE + sizeof(RouterSmem<EP>);
+}
+
+__device__ __forceinline__ void epi_bar() {  // named barrier over the 4 epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int EP>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[EP]) {
+  static_assert(EP % 16 == 0, "EP multiple of 16");
+#pragma unroll
+  for (int c = 0; c < EP; c += 32) {
+    if (c + 32 <= EP) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[c + j] = __uint_as_float(r[j]);
+    } else {
+      uint32_t r[16];
+      tmem_ld16(taddr + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[c + j] = __uint_as_float(r[j]);
+    }
+  }
+}
+
+template <int EP>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmW, const float* __restrict__ bias,
+                     const float* __restrict__ noise, float tau, int T, int d, int E, int k,
+                     float* __restrict__ logits, int32_t* __restrict__ idx,
+                     float* __restrict__ gate, float* __restrict__ partial,
+                     int32_t* __restrict__ tile_hist, int32_t* __restrict__ hdr) {
+  using Cfg = RouterCfg<EP>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  RouterSmem<EP>& st = *reinterpret_cast<RouterSmem<EP>*>(smem + STAGES * Cfg::STAGE);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&st.full[s], 1);
+      mbar_init(&st.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&st.tmem_full[a], 1);
+      mbar_init(&st.tmem_empty[a], 128);
+    }
+    mbar_init(&st.final_bar, 1);
+    st.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(&st.tmem_base, Cfg::TCOLS);
+    tmem_relinquish();
+  }
+  for (int e = tid; e < EP; e += NUM_THREADS) st.part[e] = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = st.tmem_base;
+  const int ntiles = (T + BM - 1) / BM;
+  const int num_kb = (d + BK - 1) / BK;
+  volatile int* abort_flag = &st.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, hdr, 11)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&st.full[stage], Cfg::STAGE);
+          tma_load_2d(sA + stage * A_BYTES, &tmX, &st.full[stage], kb * BK, tile * BM);
+          tma_load_2d(sB + stage * Cfg::B_BYTES, &tmW, &st.full[stage], kb * BK, 0);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (--s < 0) {
+            s = STAGES - 1;
+            ph ^= 1u;
+          }
+          volatile int no_abort = 0;
+          mbar_wait(&st.full[s], ph, &no_abort, nullptr, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, EP);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&st.tmem_empty[acc], acc_phase ^ 1u, abort_flag, hdr, 12)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * EP);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&st.full[stage], phase, abort_flag, hdr, 13)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_kmajor_sw128(a0 + stage * A_BYTES);
+          const uint64_t bdesc = sdesc_kmajor_sw128(b0 + stage * Cfg::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&st.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&st.tmem_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        umma_commit(&st.final_bar);
+        volatile int no_abort = 0;
+        mbar_wait(&st.final_bar, 0, &no_abort, nullptr, 0);
+      }
+    }
+  } else {
+    // ---------------- epilogue: thread r of the tile owns token tile*128 + r
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int etid = tid - 64;  // 0..127
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) break;
+      tc_fence_after();
+      float v[EP];
+      tmem_ld_row<EP>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * EP), v);
+      tc_fence_before();
+      mbar_arrive(&st.tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+      for (int e = etid; e < EP; e += 128) st.hist[e] = 0;
+      const int t = tile * BM + r;
+      const bool valid = t < T;
+      // selection keys
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        float z = v[e];
+        if (e < E && valid) {
+          if (bias) z += __ldg(bias + e);
+          if (noise) z += __ldg(noise + (size_t)t * E + e);
+          z = z / tau;
+        }
+        v[e] = e < E ? z : -INFINITY;
+      }
+      float m = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) m = fmaxf(m, v[e]);
+      if (valid && logits) {
+        float* lr = logits + (size_t)t * E;
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+          if (e < E) lr[e] = v[e];
+      }
+      // top-k on the keys: descending, ties to the lower index
+      uint64_t taken = 0;
+      float selv[kMaxK];
+      int seli[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        selv[j] = -INFINITY;
+        seli[j] = 0;
+        if (j < k) {
+          float bv = -INFINITY;
+          int bi = -1;
+#pragma unroll
+          for (int e = 0; e < EP; ++e) {
+            const bool free_ = e < E && !((taken >> e) & 1ull);
+            if (free_ && (bi < 0 || v[e] > bv)) {
+              bv = v[e];
+              bi = e;
+            }
+          }
+          if (bi < 0) bi = 0;
+          taken |= 1ull << bi;
+          selv[j] = bv;
+          seli[j] = bi;
+        }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        v[e] = e < E ? expf(v[e] - m) : 0.f;
+        s += v[e];
+      }
+      __syncwarp();
+      epi_bar();  // hist zeroed
+      if (valid) {
+        float psel[kMaxK], psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j < k) {
+            psel[j] = expf(selv[j] - m) / s;
+            psum += psel[j];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j < k) {
+            idx[(size_t)t * k + j] = seli[j];
+            gate[(size_t)t * k + j] = psel[j] / psum;
+            atomicAdd(&st.hist[seli[j]], 1);
+          }
+        }
+      }
+      // per-expert sums of p over the tile's tokens: butterfly in each warp,
+      // then the 4 warps in a fixed order
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        float pe = (valid && e < E) ? v[e] / s : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+        if (lane == 0) st.red[quarter][e] = pe;
+      }
+      epi_bar();
+      for (int e = etid; e < E; e += 128) {
+        st.part[e] += ((st.red[0][e] + st.red[1][e]) + st.red[2][e]) + st.red[3][e];
+        if (tile_hist) tile_hist[(size_t)tile * E + e] = st.hist[e];
+      }
+      epi_bar();
+    }
+    for (int e = etid; e < E; e += 128) partial[(size_t)blockIdx.x * E + e] = st.part[e];
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TCOLS);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_router() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool map_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn_router();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {K, rows};
+  cuuint64_t gstride[1] = {K * 2};
+  cuuint32_t box[2] = {BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EP>
+cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
+                      const float* noise, float* logits, int32_t* idx, float* gate,
+                      float* partial, int32_t* tile_hist, int32_t* hdr, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(router_tc_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)router_smem_bytes<EP>());
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  CUtensorMap mx, mw;
+  if (!map_rows(&mx, x, c.d, c.T, BM) || !map_rows(&mw, Wg, c.d, c.E, EP))
+    return cudaErrorInvalidValue;
+  router_tc_kernel<EP><<<router_tc_grid(c), NUM_THREADS, router_smem_bytes<EP>(), s>>>(
+      mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist,
+      hdr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool router_tc_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && c.E <= 64; }
+
+cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
+                             const float* bias, const float* noise, float* logits, int32_t* idx,
+                             float* gate, float* partial, int32_t* tile_hist, int32_t* hdr,
+                             cudaStream_t s) {
+  const int ep = (c.E + 15) / 16 * 16;
+  switch (ep) {
+    case 16: return launch_ep<16>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
+    case 32: return launch_ep<32>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
+    case 48: return launch_ep<48>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
+    case 64: return launch_ep<64>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe
