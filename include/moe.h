@@ -144,6 +144,28 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_i
                           int32_t *token_of_row, void *xd, void *ws, size_t ws_bytes,
                           moe_stream_t stream);
 
+/* moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory: a plugin or custom-op interface that passes only the op's own
+ * tensors, or a runtime that forbids cudaMalloc after start-up. The pages
+ * have no counterpart; this is a deployment variant of moe_dispatch with the
+ * same arguments and results, minus ws.
+ *   Scratch: a fixed 512 KiB array in the library's device memory (two int32
+ *   arrays of 65536 entries), held on every device that loaded the library
+ *   until the process exits. Returns MOE_ERR_UNSUPPORTED when
+ *   ceil(T*k / 1024) * E > 65536 (e.g. T*k > 1048576 slots at E = 64).
+ *   Allocates nothing (no cudaMalloc, no cudaFree).
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or several host threads) race and corrupt each other's results;
+ *   order them on one stream. Each call rewrites all the scratch it reads, so
+ *   leftovers of earlier calls never matter. */
+MOE_API moe_status_t moe_dispatch_static_scratch(const moe_config_t *cfg, const int32_t *topk_idx,
+                                                 const void *x, int32_t *expert_count,
+                                                 int32_t *expert_offset, int32_t *slot_of,
+                                                 int32_t *token_of_row, void *xd,
+                                                 moe_stream_t stream);
+
 /* Grouped expert FFN over the packed rows ([MoE-math] 3.1; SwiGLU for
  * act = MOE_ACT_SWIGLU). Rows [offset_e, offset_{e+1}) of xd go through expert e.
  *   xd            [T*k, d] in (dtype), first expert_offset[E] rows used
