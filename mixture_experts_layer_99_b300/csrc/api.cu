@@ -25,7 +25,7 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
   L.router_partial = take((rgrid > (size_t)kRouterTcMaxBlocks ? rgrid : kRouterTcMaxBlocks) * E * 4);
   L.router_tile_hist = take((size_t)router_tc_tiles(c) * E * 4);
   L.disp_hist = take(nblk * E * 4);
-  L.disp_base = take(nblk * E * 4);
+  L.disp_base = take((nblk > (size_t)router_tc_tiles(c) ? nblk : (size_t)router_tc_tiles(c)) * E * 4);
   L.ffn_h = take(R * (size_t)c.H * s);
   L.ffn_sched = take(4096);
   L.total_core = off;
@@ -271,18 +271,31 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
   float* partial = at<float>(ws, L.router_partial);
   float* prob_sum = at<float>(ws, L.prob_sum);
   const int64_t R = max_rows(c);
+  int32_t* token_of_row = at<int32_t>(ws, L.token_of_row);
   cudaError_t e = run_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, ws, L,
                              &rgrid, s);
-  if (e == cudaSuccess)
-    e = launch_dispatch(c, idx, x, count, offset, slot_of, at<int32_t>(ws, L.token_of_row),
-                        at<void>(ws, L.xd), at<int32_t>(ws, L.disp_hist),
-                        at<int32_t>(ws, L.disp_base), R, s);
+  const bool fused_stats = router_tc_supported(c);
+  if (e == cudaSuccess) {
+    if (fused_stats) {
+      // the router's per-tile histograms and probability partials feed one
+      // scan + statistics kernel and a per-tile position kernel
+      e = launch_dispatch_from_router(c, idx, at<int32_t>(ws, L.router_tile_hist), partial,
+                                      rgrid, at<int32_t>(ws, L.disp_base), count, offset,
+                                      slot_of, token_of_row, prob_sum, f, P, Lb, dropped, s);
+      if (e == cudaSuccess) e = launch_gather(c, x, token_of_row, offset, at<void>(ws, L.xd), R, s);
+    } else {
+      e = launch_dispatch(c, idx, x, count, offset, slot_of, token_of_row, at<void>(ws, L.xd),
+                          at<int32_t>(ws, L.disp_hist), at<int32_t>(ws, L.disp_base), R, s);
+    }
+  }
   if (e == cudaSuccess)
     e = launch_ffn(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
                    at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s);
   if (e == cudaSuccess) e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s);
-  if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
-  if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
+  if (!fused_stats) {
+    if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
+    if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
+  }
   return cuda_status(e);
 }
 
@@ -307,9 +320,10 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const moe_layer_inputs_t
 
 int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
-  // router, dispatch (count, scan, assign, gather), GEMM1, GEMM2, combine,
-  // probability reduction, statistics
-  return 10;
+  // tensor-core router path: router, scan + statistics, assign, gather,
+  // GEMM1, GEMM2, combine. FMA router path: router, dispatch (count, scan,
+  // assign, gather), GEMM1, GEMM2, combine, probability reduction, statistics.
+  return router_tc_supported(*cfg) ? 7 : 10;
 }
 
 moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,

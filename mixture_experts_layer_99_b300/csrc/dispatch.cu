@@ -154,6 +154,17 @@ __global__ void __launch_bounds__(NT) disp_gather_kernel(const uint4* __restrict
 
 }  // namespace
 
+cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* token_of_row,
+                          const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s) {
+  const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
+  const int64_t gblk = (rows_bound + NW - 1) / NW;
+  if (gblk > 0)
+    disp_gather_kernel<<<(unsigned)gblk, NT, 0, s>>>(static_cast<const uint4*>(x),
+                                                     token_of_row, offset, c.E, nvec,
+                                                     static_cast<uint4*>(xd));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,
                             int32_t* count, int32_t* offset, int32_t* slot_of,
                             int32_t* token_of_row, void* xd, int32_t* hist, int32_t* base,
