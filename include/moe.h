@@ -232,6 +232,19 @@ MOE_API moe_status_t moe_layer_forward(const moe_config_t *cfg, const moe_layer_
                                const moe_layer_outputs_t *out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* moe_layer_forward with timing marks: stage_events points to six
+ * cudaEvent_t handles (created by the caller, timing enabled) that are
+ * recorded on `stream` before the router, after the router, after the
+ * dispatch, after GEMM1 (the hidden activation), after GEMM2 and after the
+ * combine and statistics. Where a path has no boundary between two marks
+ * (the fp32 path runs both GEMMs in one call) both are recorded at the same
+ * point. Results are identical to moe_layer_forward. */
+MOE_API moe_status_t moe_layer_forward_profiled(const moe_config_t *cfg,
+                                                const moe_layer_inputs_t *in,
+                                                const moe_layer_outputs_t *out, void *ws,
+                                                size_t ws_bytes, moe_stream_t stream,
+                                                void *const *stage_events);
+
 /* Number of kernels one moe_layer_forward call launches for this shape
  * (0 if cfg is invalid). Host only. */
 MOE_API int32_t moe_layer_forward_launch_count(const moe_config_t *cfg);

@@ -251,10 +251,15 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* expert_count,
                                 dropped, (cudaStream_t)stream));
 }
 
+// ev (optional): six events recorded on s at the stage boundaries: before
+// the router, after the router, after the dispatch, after GEMM1, after GEMM2,
+// after the combine and statistics.
 static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
                                        const moe_layer_inputs_t* in,
                                        const moe_layer_outputs_t* out, void* y, float* Lout,
-                                       void* ws, cudaStream_t s) {
+                                       void* ws, cudaStream_t s,
+                                       const cudaEvent_t* ev = nullptr) {
+  auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
   const moe_config_t& c = *cfg;
   const WsLayout L = ws_layout(c, 0);
   int32_t* idx = out && out->topk_idx ? out->topk_idx : at<int32_t>(ws, L.topk_idx);
@@ -272,30 +277,53 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
   float* prob_sum = at<float>(ws, L.prob_sum);
   const int64_t R = max_rows(c);
   int32_t* token_of_row = at<int32_t>(ws, L.token_of_row);
-  cudaError_t e = run_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, ws, L,
-                             &rgrid, s);
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess)
+    e = run_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, ws, L, &rgrid, s);
+  if (e == cudaSuccess) e = mark(1);
+  // tensor-core router (bf16, E <= 64): its per-tile histograms and
+  // probability partials feed one scan + statistics kernel and a per-tile
+  // position kernel; for k = 1 GEMM2 writes the gated rows straight into y.
   const bool fused_stats = router_tc_supported(c);
+  const bool scatter = fused_stats && c.k == 1;
   if (e == cudaSuccess) {
     if (fused_stats) {
-      // the router's per-tile histograms and probability partials feed one
-      // scan + statistics kernel and a per-tile position kernel
       e = launch_dispatch_from_router(c, idx, at<int32_t>(ws, L.router_tile_hist), partial,
                                       rgrid, at<int32_t>(ws, L.disp_base), count, offset,
-                                      slot_of, token_of_row, prob_sum, f, P, Lb, dropped, s);
+                                      slot_of, token_of_row, prob_sum, f, P, Lb, dropped,
+                                      scatter ? y : nullptr, s);
       if (e == cudaSuccess) e = launch_gather(c, x, token_of_row, offset, at<void>(ws, L.xd), R, s);
     } else {
       e = launch_dispatch(c, idx, x, count, offset, slot_of, token_of_row, at<void>(ws, L.xd),
                           at<int32_t>(ws, L.disp_hist), at<int32_t>(ws, L.disp_base), R, s);
     }
   }
-  if (e == cudaSuccess)
-    e = launch_ffn(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
-                   at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s);
-  if (e == cudaSuccess) e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess) {
+    if (fused_stats) {
+      FfnFusion fz;
+      fz.between = ev ? ev[3] : nullptr;
+      if (scatter) {
+        fz.y = y;
+        fz.scatter_rows = token_of_row;
+        fz.scatter_scale = gate;
+      }
+      e = launch_ffn_tc(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
+                        at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s,
+                        &fz);
+    } else {
+      e = launch_ffn(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
+                     at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s);
+      if (e == cudaSuccess) e = mark(3);  // the FMA path has no mark between its GEMMs
+    }
+  }
+  if (e == cudaSuccess) e = mark(4);
+  if (e == cudaSuccess && !scatter) e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s);
   if (!fused_stats) {
     if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
     if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
   }
+  if (e == cudaSuccess) e = mark(5);
   return cuda_status(e);
 }
 
@@ -318,12 +346,30 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const moe_layer_inputs_t
                             (cudaStream_t)stream);
 }
 
+moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                        const moe_layer_outputs_t* out, void* ws,
+                                        size_t ws_bytes, moe_stream_t stream,
+                                        void* const* stage_events) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if (!in->x || !out || !out->y || !stage_events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!stage_events[i]) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg, 0).total_layer)) != MOE_OK) return st;
+  return layer_forward_impl(cfg, in->x, in, out, out->y, out->L_balance, ws,
+                            (cudaStream_t)stream,
+                            reinterpret_cast<const cudaEvent_t*>(stage_events));
+}
+
 int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
   // tensor-core router path: router, scan + statistics, assign, gather,
-  // GEMM1, GEMM2, combine. FMA router path: router, dispatch (count, scan,
-  // assign, gather), GEMM1, GEMM2, combine, probability reduction, statistics.
-  return router_tc_supported(*cfg) ? 7 : 10;
+  // GEMM1, GEMM2, and the combine unless k = 1 (then GEMM2 writes y). FMA
+  // router path: router, dispatch (count, scan, assign, gather), GEMM1, GEMM2,
+  // combine, probability reduction, statistics.
+  if (router_tc_supported(*cfg)) return cfg->k == 1 ? 6 : 7;
+  return 10;
 }
 
 moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,

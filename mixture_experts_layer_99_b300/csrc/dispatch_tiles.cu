@@ -93,10 +93,13 @@ __global__ void __launch_bounds__(1024) scan_stats_kernel(
 
 // One block of 256 threads per 128-token tile; warp w owns tokens
 // [16w, 16w + 16) of the tile, i.e. 16k consecutive slots, walked 32 at a time.
+// With zero_y (k = 1 only), the y row of every token whose slot was dropped
+// is cleared here, because the expert FFN then writes y only for kept tokens.
 __global__ void __launch_bounds__(256) assign_tiles_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, int C,
     const int32_t* __restrict__ base, const int32_t* __restrict__ offset,
-    int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row) {
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row,
+    uint4* __restrict__ zero_y, int y_vec16) {
   __shared__ int wcnt[8][kMaxE];
   __shared__ int offs[kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -137,13 +140,23 @@ __global__ void __launch_bounds__(256) assign_tiles_kernel(
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) wcnt[w][e] += __popc(peers);
     __syncwarp();
+    int32_t row = -1;
     if (in) {
-      int32_t row = -1;
       if (valid && pos < C) {
         row = offs[e] + pos;
         token_of_row[row] = (int32_t)(s / k);
       }
       slot_of[s] = row;
+    }
+    if (zero_y) {
+      unsigned drop = __ballot_sync(0xffffffffu, in && row < 0);
+      while (drop) {
+        const int l = __ffs(drop) - 1;
+        drop &= drop - 1;
+        const int64_t t = s0 + c + l;  // k = 1: slot index = token index
+        uint4* yr = zero_y + (size_t)t * y_vec16;
+        for (int v = lane; v < y_vec16; v += 32) yr[v] = make_uint4(0, 0, 0, 0);
+      }
     }
   }
 }
@@ -156,13 +169,16 @@ cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* id
                                         int32_t* offset, int32_t* slot_of,
                                         int32_t* token_of_row, float* prob_sum, float* f,
                                         float* P, float* Lb, int32_t* dropped,
-                                        cudaStream_t s) {
+                                        void* zero_y, cudaStream_t s) {
   const int ntiles = router_tc_tiles(c);
   scan_stats_kernel<<<1, 1024, 0, s>>>(tile_hist, ntiles, partial, nparts, c.T, c.E, c.k,
                                        c.capacity, base, count, offset, prob_sum, f, P, Lb,
                                        dropped);
+  const int y_vec16 = (int)((size_t)c.d * elem_bytes(c) / 16);
   assign_tiles_kernel<<<ntiles, 256, 0, s>>>(idx, c.T, c.k, c.E, c.capacity, base, offset,
-                                             slot_of, token_of_row);
+                                             slot_of, token_of_row,
+                                             c.k == 1 ? static_cast<uint4*>(zero_y) : nullptr,
+                                             y_vec16);
   return cudaGetLastError();
 }
 

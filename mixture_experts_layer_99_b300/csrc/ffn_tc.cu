@@ -21,6 +21,13 @@
 // GEMM1 (SwiGLU): B tile = 128 rows of W1 then the same 128 rows of W3, so one
 //                 N = 256 MMA yields gate and up: h = silu(gate) * up   tile N = 128
 // GEMM2:          Y[r, n] = sum_k h[r,k] W2[e,n,k] (+ b2[e,n])        tile N = 256
+//
+// Inside the fused layer call, for k = 1 every token has at most one kept
+// slot, so GEMM2 (SCATTER) scales its row by the gate and writes
+// y[token_of_row[r]] directly: the combine y_t = g_t E(x_t) of the kwkr.cn
+// article, section 2.1, with no Y buffer and no combine kernel. (Gathering
+// GEMM1's A rows by token with TMA gather4 instead of a packed copy was
+// measured 2x slower on B300: 33 TMA operations per K step instead of 2.)
 #include "moe_internal.h"
 #include "tc_ptx.cuh"
 
@@ -60,10 +67,28 @@ struct SmemTail {
 
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + sizeof(SmemTail);
 
-__device__ __forceinline__ float gelu_erf(float u) {
-  return 0.5f * u * (1.f + erff(u * 0.70710678118654752f));
+// GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
+// approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (Hastings): for z >= 0, erf(z) = 1 - q(z) with
+// q(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2), t = 1/(1 + p z),
+// |error| <= 1.5e-7. Written as GELU(u) = u - u q / 2 for u >= 0 and u q / 2
+// for u < 0, so there is neither a branch (all lanes of a warp take the same
+// path) nor a cancellation for negative u.
+__device__ __forceinline__ float gelu_as(float u) {
+  const float z = fabsf(u) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float q = poly * __expf(-z * z);
+  const float half_uq = 0.5f * u * q;
+  return u >= 0.f ? u - half_uq : half_uq;
 }
-__device__ __forceinline__ float silu_f(float u) { return u / (1.f + expf(-u)); }
+// silu(u) = u / (1 + exp(-u)); for large negative u the denominator
+// overflows to +inf and the quotient is 0.
+__device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
 struct TileInfo {
   int e, m0, mend, n0;
@@ -89,14 +114,16 @@ __device__ __forceinline__ TileInfo tile_info(const SmemTail& st, int E, int n_t
   return ti;
 }
 
-template <int MODE>
+template <int MODE, bool SCATTER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB3,
                            const int32_t* __restrict__ offset, int E, int N, int K,
                            const __nv_bfloat16* __restrict__ bias,
-                           __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr) {
+                           __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
+                           const int32_t* __restrict__ o_rows,
+                           const float* __restrict__ o_scale) {
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -161,7 +188,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = &st.abort_flag;
 
   if (warp == 0) {
-    // ================= TMA producer
+    // ================= TMA producer (lane 0)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -269,7 +296,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = ti.m0 + quarter * 32 + lane;
       const bool row_ok = row < ti.mend;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * UMMA_N);
-      __nv_bfloat16* orow = out + (size_t)row * N;
+      int orow_idx = row;
+      float oscale = 1.f;
+      if (SCATTER) {
+        orow_idx = row_ok ? __ldg(o_rows + row) : 0;
+        oscale = row_ok ? __ldg(o_scale + orow_idx) : 0.f;
+      }
+      __nv_bfloat16* orow = out + (size_t)orow_idx * N;
       constexpr int CHUNKS = (MODE == kSwiglu ? 64 : 128) / 32;
 #pragma unroll 1
       for (int ch = 0; ch < CHUNKS; ++ch) {
@@ -297,8 +330,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (MODE == kGelu) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+            for (int j = 0; j < 32; ++j) v[j] = gelu_as(v[j]);
           }
+        }
+        if (SCATTER) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= oscale;
         }
         if (row_ok) {
 #pragma unroll
@@ -377,16 +414,17 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint6
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool SCATTER>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                         const int32_t* offset, int E, int N, int K, const void* bias, void* out,
-                        int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
+                        int64_t rows_bound, int32_t* hdr, const int32_t* o_rows,
+                        const float* o_scale, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+    e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, SCATTER>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -395,9 +433,9 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   const int64_t tiles_bound = ((rows_bound + BM - 1) / BM + E) * ((N + BN_OUT - 1) / BN_OUT);
   const int sms = device_sm_count();
   const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
-  grouped_gemm_tc_kernel<MODE><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
+  grouped_gemm_tc_kernel<MODE, SCATTER><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
       a, b, b3, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
-      static_cast<__nv_bfloat16*>(out), hdr);
+      static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale);
   return cudaGetLastError();
 }
 
@@ -406,10 +444,11 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                           const void* W1, const void* W3, const void* W2, const void* b1,
                           const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
-                          cudaStream_t s) {
+                          cudaStream_t s, const FfnFusion* fz) {
   CUtensorMap mx, mh, mw1, mw3, mw2;
   const uint64_t R = (uint64_t)rows_bound;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  const bool scatter = fz && fz->scatter_rows;
   if (!make_map_2d(&mx, xd, c.d, R) || !make_map_2d(&mh, h, c.H, R) ||
       !make_map_3d(&mw1, W1, c.d, c.H, c.E, swiglu ? 128 : UMMA_N) ||
       !make_map_3d(&mw2, W2, c.H, c.d, c.E, UMMA_N))
@@ -418,12 +457,19 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
   if (!swiglu) mw3 = mw1;
   cudaError_t e;
   if (swiglu)
-    e = launch_gemm<kSwiglu>(mx, mw1, mw3, offset, c.E, c.H, c.d, nullptr, h, rows_bound, hdr, s);
+    e = launch_gemm<kSwiglu, false>(mx, mw1, mw3, offset, c.E, c.H, c.d, nullptr, h, rows_bound,
+                                    hdr, nullptr, nullptr, s);
   else
-    e = launch_gemm<kGelu>(mx, mw1, mw3, offset, c.E, c.H, c.d, b1, h, rows_bound, hdr, s);
+    e = launch_gemm<kGelu, false>(mx, mw1, mw3, offset, c.E, c.H, c.d, b1, h, rows_bound, hdr,
+                                  nullptr, nullptr, s);
   if (e != cudaSuccess) return e;
-  return launch_gemm<kPlain>(mh, mw2, mw2, offset, c.E, c.d, c.H, swiglu ? nullptr : b2, Y,
-                             rows_bound, hdr, s);
+  if (fz && fz->between && (e = cudaEventRecord(fz->between, s)) != cudaSuccess) return e;
+  const void* b2e = swiglu ? nullptr : b2;
+  if (scatter)
+    return launch_gemm<kPlain, true>(mh, mw2, mw2, offset, c.E, c.d, c.H, b2e, fz->y, rows_bound,
+                                     hdr, fz->scatter_rows, fz->scatter_scale, s);
+  return launch_gemm<kPlain, false>(mh, mw2, mw2, offset, c.E, c.d, c.H, b2e, Y, rows_bound, hdr,
+                                    nullptr, nullptr, s);
 }
 
 }  // namespace moe

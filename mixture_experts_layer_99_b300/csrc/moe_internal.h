@@ -101,7 +101,8 @@ cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* id
                                         int nparts, int32_t* base, int32_t* count,
                                         int32_t* offset, int32_t* slot_of,
                                         int32_t* token_of_row, float* prob_sum, float* f,
-                                        float* P, float* Lb, int32_t* dropped, cudaStream_t s);
+                                        float* P, float* Lb, int32_t* dropped, void* zero_y,
+                                        cudaStream_t s);
 cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
                        const void* W1, const void* W3, const void* W2, const void* b1,
                        const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
@@ -110,10 +111,18 @@ cudaError_t launch_ffn_simt(const moe_config_t& c, const void* xd, const int32_t
                             const void* W1, const void* W3, const void* W2, const void* b1,
                             const void* b2, void* Y, void* h, int64_t rows_bound,
                             cudaStream_t s);
+// Fusion of the tensor-core FFN inside the fused layer call: for k = 1 GEMM2
+// writes gate * row straight to y[token] (no Y buffer, no combine).
+struct FfnFusion {
+  void* y = nullptr;                      // [T, d] layer output
+  const int32_t* scatter_rows = nullptr;  // token_of_row, or nullptr (k = 1 only)
+  const float* scatter_scale = nullptr;   // topk_gate [T] (k = 1)
+  cudaEvent_t between = nullptr;          // recorded between GEMM1 and GEMM2, if set
+};
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                           const void* W1, const void* W3, const void* W2, const void* b1,
                           const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
-                          cudaStream_t s);
+                          cudaStream_t s, const FfnFusion* fz = nullptr);
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
                            const float* gate, void* y, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,

@@ -29,7 +29,7 @@ EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspa
             "moe_workspace_size_host", "moe_workspace_init", "moe_device_status",
             "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
             "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
-            "moe_layer_forward_launch_count"]
+            "moe_layer_forward_launch_count", "moe_layer_forward_profiled"]
 
 
 class MoEError(RuntimeError):
@@ -92,6 +92,9 @@ def lib():
         "moe_layer_forward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs),
                                         vp, c_size_t, vp]),
         "moe_layer_forward_launch_count": (c_int32, [cfgp]),
+        "moe_layer_forward_profiled": (c_int32, [cfgp, POINTER(LayerInputs),
+                                                 POINTER(LayerOutputs), vp, c_size_t, vp,
+                                                 POINTER(c_void_p)]),
         "moe_layer_forward_host": (c_int32, [cfgp, vp, POINTER(LayerInputs), vp, vp, vp,
                                              c_size_t, vp]),
     }
@@ -319,6 +322,18 @@ def layer_forward(cfg, inp: dict, *, ws=None, out: Optional[dict] = None, full=T
     ws = workspace(cfg, dev) if ws is None else ws
     _call("moe_layer_forward", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(lo),
           _ptr(ws), ws.numel(), _stream(dev))
+    return out
+
+
+def layer_forward_profiled(cfg, inp: dict, events, *, ws, out: dict):
+    """moe_layer_forward that records six torch.cuda.Event (timing enabled,
+    already recorded once so that they exist) at the stage boundaries."""
+    dev = inp["x"].device
+    li = _layer_inputs(cfg, inp, dev)
+    lo = LayerOutputs(*[_ptr(out.get(n)) for n, _ in LayerOutputs._fields_])
+    arr = (c_void_p * 6)(*[c_void_p(e.cuda_event) for e in events])
+    _call("moe_layer_forward_profiled", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(lo),
+          _ptr(ws), ws.numel(), _stream(dev), arr)
     return out
 
 

@@ -121,3 +121,18 @@ def test_workspace_checks():
     assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), None, need, None) == 3
     assert L.moe_router_topk(r, fake, fake, None, None, None, fake, fake, fake, fake, 16,
                              None) == 3
+
+
+def test_launch_count_matches_path():
+    """Kernels per moe_layer_forward: 6 (tensor-core router, k = 1: GEMM2
+    writes y), 7 (tensor-core router, k > 1), 10 (fp32 or E > 64)."""
+    from mixture_experts_layer_99_b300 import workloads as W
+    L = moe.lib()
+    cases = [(W.WORKLOADS["switch_top1"], 6), (W.WORKLOADS["longtail"], 7),
+             (W.WORKLOADS["mixtral"], 7), (W.WORKLOADS["ref_fp32"], 10),
+             (W.small(W.WORKLOADS["switch_top1"], T=64, d=64, H=64, E=128, k=2), 10)]
+    for w, want in cases:
+        cfg = moe.config_from_workload(w)
+        assert L.moe_layer_forward_launch_count(ctypes.byref(cfg)) == want, w.name
+    bad = _cfg(T=0)
+    assert L.moe_layer_forward_launch_count(ctypes.byref(bad)) == 0

@@ -92,3 +92,25 @@ def test_layer_zero_router_closed_form():
     assert out["dropped"].item() == 2 * (600 - C)
     r = ORC.moe_forward(inp, k=2, c=w.c, act=w.act, tokens=np.arange(C))
     assert rel_err(np_of(out["y"][:C]), r["y"]) <= TOL_Y["bf16"]
+
+
+@pytest.mark.parametrize("name", ["switch_small", "longtail_small", "ref_fp32"])
+def test_layer_profiled_matches_and_times(name):
+    """moe_layer_forward_profiled gives the same results as moe_layer_forward
+    and records six ordered stage events."""
+    w = SMALL[name]
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(W.make_inputs(w), DEV)
+    a = moe.layer_forward(cfg, dinp)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record()
+    b = moe.layer_forward_profiled(cfg, dinp, evs, ws=moe.workspace(cfg, DEV),
+                                   out=moe.alloc_outputs(cfg, DEV))
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in times)
+    assert evs[0].elapsed_time(evs[5]) > 0
+

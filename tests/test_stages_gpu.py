@@ -204,3 +204,45 @@ def test_workspace_status_clean_after_calls():
     inp = W.to_device(W.make_inputs(w), DEV)
     moe.layer_forward(cfg, inp, ws=ws)
     assert moe.device_status(ws) == (0, 0)
+
+
+def _bf16_ulp(v):
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(v), 1e-30)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_tensor_core_activation_accuracy(act):
+    """Identity expert weights make Y = bf16(act(x)) exactly (fp32 sums of
+    x * 1 are exact), so the device activation can be checked element by
+    element against the exact one: the only allowed error is the final bf16
+    rounding plus a slack far below it (4e-6 relative for the fast exp and
+    division, 3e-7 absolute per unit of |u| for the erf approximation, whose
+    bound is 1.5e-7). A tanh-form GELU (error ~1e-3) would fail."""
+    d = H = 256
+    R = 1024
+    g = torch.Generator().manual_seed(21)
+    xv = torch.linspace(-9.0, 9.0, R * d - 6, dtype=torch.float64)
+    xv = torch.cat([xv, torch.tensor([0.0, 1e-6, -1e-6, 30.0, -30.0, -100.0],
+                                     dtype=torch.float64)])
+    xv = xv[torch.randperm(xv.numel(), generator=g)]
+    x = xv.reshape(R, d).to(torch.bfloat16)
+    eye = torch.eye(d, dtype=torch.bfloat16)
+    W1 = eye[None].clone()
+    W2 = eye[None].clone()
+    W3 = eye[None].clone() if act == "swiglu" else None
+    cfg = moe.make_config(R, d, 1, 1, H, R, "bf16", act)
+    off = torch.tensor([0, R], dtype=torch.int32, device=DEV)
+    Y = moe.expert_ffn(cfg, x.to(DEV), off, W1.to(DEV), W2.to(DEV),
+                       None if W3 is None else W3.to(DEV))
+    torch.cuda.synchronize()
+    u = x.double().numpy()
+    if act == "gelu":
+        exact = ORC.gelu(u)
+    else:
+        exact = ORC.silu(u) * u
+    y = Y.double().cpu().numpy()
+    bound = 0.5 * _bf16_ulp(exact) + 4e-6 * np.abs(exact) + 3e-7 * np.maximum(1.0, np.abs(u))
+    bad = np.abs(y - exact) > bound
+    assert not bad.any(), (u[bad][:5], y[bad][:5], exact[bad][:5])
