@@ -243,6 +243,10 @@ def main():
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    # all work on one non-default stream (CUDA graphs cannot be captured on
+    # the legacy default stream)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     pg = None
     if world > 1:
         import torch.distributed as dist
@@ -260,7 +264,6 @@ def main():
     cfg = moe.config_from_workload(w)
     ws = moe.workspace(cfg, dev, host_io=True)
     out = moe.alloc_outputs(cfg, dev, full=True)
-    stream = torch.cuda.current_stream(dev)
 
     # ---- routing statistics of set 0 (for the algorithmic work model)
     moe.layer_forward(cfg, sets[0], ws=ws, out=out)
@@ -270,8 +273,25 @@ def main():
     n_active = int((np.diff(offs) > 0).sum())
     work = algorithmic(w, kept, n_active)
 
-    def step(i):
+    def step_eager(i):
         moe.layer_forward(cfg, sets[i % nsets], ws=ws, out=out)
+
+    for i in range(args.warmup):
+        step_eager(i)
+    torch.cuda.synchronize(dev)
+    # one CUDA graph per input set, each holding one layer call; a step
+    # replays the next set's graph (the same kernels and arguments as the
+    # eager call, without the host launch overhead)
+    graphs = []
+    for i in range(nsets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_eager(i)
+        graphs.append(g)
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        graphs[i % nsets].replay()
 
     for i in range(args.warmup):
         step(i)
@@ -298,54 +318,30 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     value = w.T * world / (ms / 1e3)
+    # the same K steps as direct (eager) calls, for comparison
+    ev0.record(stream)
+    for i in range(args.steps):
+        step_eager(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
     status = moe.device_status(ws)
 
-    # ---- per-stage timing (same rotation; each stage alone, events on this stream)
-    st = {}
-    reps = max(20, min(args.steps, 200))
-    dinp = sets
-    lg, idx, gate, psum = (out["logits"], out["topk_idx"], out["topk_gate"],
-                           torch.empty(cfg.E, dtype=torch.float32, device=dev))
-    rows = min(cfg.T * cfg.k, cfg.E * cfg.capacity)
-    xd = torch.empty(cfg.T * cfg.k, cfg.d, dtype=sets[0]["x"].dtype, device=dev)
-    Yb = torch.empty_like(xd)
-    disp = moe.dispatch(cfg, idx, sets[0]["x"], ws=ws)
-
-    def timed(fn):
-        for i in range(3):
-            fn(i)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(reps):
-            fn(i)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / reps
-
-    st["router"] = timed(lambda i: moe._call(
-        "moe_router_topk", moe.ctypes.byref(cfg), dinp[i % nsets]["x"].data_ptr(),
-        dinp[i % nsets]["Wg"].data_ptr(), moe._ptr(dinp[i % nsets]["bias"]),
-        moe._ptr(dinp[i % nsets]["noise"]), lg.data_ptr(), idx.data_ptr(), gate.data_ptr(),
-        psum.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream))
-    st["dispatch"] = timed(lambda i: moe._call(
-        "moe_dispatch", moe.ctypes.byref(cfg), idx.data_ptr(), dinp[i % nsets]["x"].data_ptr(),
-        disp["count"].data_ptr(), disp["offset"].data_ptr(), disp["slot_of"].data_ptr(),
-        disp["token_of_row"].data_ptr(), xd.data_ptr(), ws.data_ptr(), ws.numel(),
-        stream.cuda_stream))
-    st["expert_ffn"] = timed(lambda i: moe._call(
-        "moe_expert_ffn", moe.ctypes.byref(cfg), xd.data_ptr(), disp["offset"].data_ptr(),
-        dinp[i % nsets]["W1"].data_ptr(), moe._ptr(dinp[i % nsets]["W3"]),
-        dinp[i % nsets]["W2"].data_ptr(), moe._ptr(dinp[i % nsets]["b1"]),
-        moe._ptr(dinp[i % nsets]["b2"]), Yb.data_ptr(), ws.data_ptr(), ws.numel(),
-        stream.cuda_stream))
-    st["combine"] = timed(lambda i: moe._call(
-        "moe_combine", moe.ctypes.byref(cfg), Yb.data_ptr(), disp["slot_of"].data_ptr(),
-        gate.data_ptr(), out["y"].data_ptr(), stream.cuda_stream))
-    st["aux_stats"] = timed(lambda i: moe._call(
-        "moe_aux_stats", moe.ctypes.byref(cfg), disp["count"].data_ptr(), psum.data_ptr(),
-        out["f"].data_ptr(), out["P"].data_ptr(), out["L_balance"].data_ptr(),
-        out["dropped"].data_ptr(), stream.cuda_stream))
+    # ---- live stage times: the same steps through moe_layer_forward_profiled,
+    # which records CUDA events on this stream at the stage boundaries
+    prof_steps = max(10, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(prof_steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # create the events
+    torch.cuda.synchronize(dev)
+    for i in range(prof_steps):
+        moe.layer_forward_profiled(cfg, sets[i % nsets], evs[i], ws=ws, out=out)
+    torch.cuda.synchronize(dev)
+    names = ["router", "dispatch", "gemm1", "gemm2", "combine_stats"]
+    st = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(prof_steps)) / prof_steps
+          for j, n in enumerate(names)}
+    st["layer"] = sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(prof_steps)) / prof_steps
 
     # ---- end to end through the host-buffer C call (pinned host x and y)
     xh = [s["x"].cpu().pin_memory() for s in sets[:2]]
@@ -371,16 +367,23 @@ def main():
     bytes_x = cfg.T * cfg.d * sets[0]["x"].element_size()
 
     # ---- roofline of the dominant kernel (the grouped GEMM, two launches per call)
-    gemm_ms = st["expert_ffn"]
+    gemm_ms = st["gemm1"] + st["gemm2"]
     achieved = work["gemm_flops"] / (gemm_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
     rec = traffic_record(source_sha())
-    roof = dict(kernel="grouped_gemm_tc_kernel (GEMM1 + GEMM2 launches)", bound="tensor",
-                achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
-                peak_source=f"{peaks['source']} burst bf16",
+    g1_flops = work["gemm_flops"] * (w.nmat - 1) / w.nmat
+    g2_flops = work["gemm_flops"] / w.nmat
+    roof = dict(kernel="grouped_gemm_tc_kernel (GEMM1 + GEMM2 launches per layer call)",
+                bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
+                frac=achieved / peak,
+                peak_source=f"{peaks['source']} burst bf16 (MEASURED_PEAKS.json)",
                 traffic=None if rec is None else rec["bytes_per_launch"],
                 algorithmic_flops_per_launch=work["gemm_flops"] / 2,
-                launch_ms=gemm_ms / 2)
+                launch_ms=gemm_ms / 2,
+                gemm1=dict(ms=st["gemm1"], tflops=g1_flops / (st["gemm1"] / 1e3) / 1e12),
+                gemm2=dict(ms=st["gemm2"], tflops=g2_flops / (st["gemm2"] / 1e3) / 1e12),
+                frac_of_sustained=(achieved / peaks["bf16_tflops_sustained"]
+                                   if peaks.get("bf16_tflops_sustained") else None))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -391,12 +394,14 @@ def main():
         hbm = peaks["hbm_gbs"]
         line = dict(
             metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
-            warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+            warmup=args.warmup, ms_per_step=ms, eager_ms_per_step=eager_ms,
+            higher_is_better=True, scaling="weak",
             vs_baseline=None, dtype="bf16" if w.dtype == "bf16" else "f32",
             data="synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
             config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
                         capacity=cfg.capacity, kept_rows=kept, active_experts=n_active,
                         parallelism=f"replicas x{world}",
+                        launch="one CUDA graph per input set, one layer call each",
                         l2=f"{nsets} rotating input+weight sets of {fp / 2**20:.0f} MiB "
                            f"(> L2 between reuses)"),
             roofline=roof,
@@ -410,13 +415,12 @@ def main():
             stages_roofline=dict(
                 router_gbs=work["router_bytes"] / (st["router"] / 1e3) / 1e9,
                 router_hbm_frac=work["router_bytes"] / (st["router"] / 1e3) / 1e9 / hbm,
-                dispatch_gbs=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9,
-                dispatch_hbm_frac=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9 / hbm,
-                combine_gbs=work["combine_bytes"] / (st["combine"] / 1e3) / 1e9,
-                combine_hbm_frac=work["combine_bytes"] / (st["combine"] / 1e3) / 1e9 / hbm,
                 gemm_tflops=achieved, gemm_frac_burst=achieved / peak,
                 gemm_weight_gbs=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9,
-                hbm_peak_gbs=hbm),
+                gemm_weight_hbm_frac=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9 / hbm,
+                hbm_peak_gbs=hbm,
+                note="stage times from moe_layer_forward_profiled events; the fused path "
+                     "gathers token rows inside GEMM1 and (k = 1) combines inside GEMM2"),
             device_status=status[0],
         )
         print(json.dumps(line), flush=True)
