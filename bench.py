@@ -419,8 +419,8 @@ def main():
                 gemm_weight_gbs=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9,
                 gemm_weight_hbm_frac=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9 / hbm,
                 hbm_peak_gbs=hbm,
-                note="stage times from moe_layer_forward_profiled events; the fused path "
-                     "gathers token rows inside GEMM1 and (k = 1) combines inside GEMM2"),
+                note="stage times from moe_layer_forward_profiled events; for k = 1 the "
+                     "combine runs inside GEMM2"),
             device_status=status[0],
         )
         print(json.dumps(line), flush=True)

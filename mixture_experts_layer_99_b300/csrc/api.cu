@@ -24,6 +24,10 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
   L.hdr = take(kHdrBytes);
   L.router_partial = take((rgrid > (size_t)kRouterTcMaxBlocks ? rgrid : kRouterTcMaxBlocks) * E * 4);
   L.router_tile_hist = take((size_t)router_tc_tiles(c) * E * 4);
+  {
+    const RouterSplit sp = router_tc_split(c);
+    L.router_split = take(sp.ksplit > 1 ? (size_t)sp.ksplit * T * E * 4 : 4);
+  }
   L.disp_hist = take(nblk * E * 4);
   L.disp_base = take((nblk > (size_t)router_tc_tiles(c) ? nblk : (size_t)router_tc_tiles(c)) * E * 4);
   L.ffn_h = take(R * (size_t)c.H * s);
@@ -65,9 +69,10 @@ cudaError_t run_router(const moe_config_t& c, const void* x, const void* Wg, con
                        void* ws, const WsLayout& L, int* nparts, cudaStream_t s) {
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.router_partial);
   if (router_tc_supported(c)) {
-    *nparts = router_tc_grid(c);
+    *nparts = router_tc_nparts(c);
     return launch_router_tc(c, x, Wg, bias, noise, logits, idx, gate, partial,
                             reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.router_tile_hist),
+                            reinterpret_cast<float*>(static_cast<char*>(ws) + L.router_split),
                             reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hdr), s);
   }
   *nparts = router_grid(c, 0);
@@ -364,11 +369,13 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const moe_layer
 
 int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
-  // tensor-core router path: router, scan + statistics, assign, gather,
-  // GEMM1, GEMM2, and the combine unless k = 1 (then GEMM2 writes y). FMA
+  // tensor-core router path: router (two kernels when its K range is split),
+  // scan + statistics, assign, gather, GEMM1, GEMM2, and the combine unless
+  // k = 1 (then GEMM2 writes y). FMA
   // router path: router, dispatch (count, scan, assign, gather), GEMM1, GEMM2,
   // combine, probability reduction, statistics.
-  if (router_tc_supported(*cfg)) return cfg->k == 1 ? 6 : 7;
+  if (router_tc_supported(*cfg))
+    return (cfg->k == 1 ? 6 : 7) + (router_tc_split(*cfg).ksplit > 1 ? 1 : 0);
   return 10;
 }
 

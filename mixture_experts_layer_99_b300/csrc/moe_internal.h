@@ -57,6 +57,24 @@ inline int router_tc_grid(const moe_config_t& c) {
   const int t = router_tc_tiles(c);
   return t < kRouterTcMaxBlocks ? t : kRouterTcMaxBlocks;
 }
+// With fewer tiles than SMs the router splits each tile's K range (64-wide
+// blocks) over ksplit CTAs; ksplit * tiles <= 148 and every split is non-empty.
+struct RouterSplit {
+  int ksplit, kb_per_split;
+};
+inline RouterSplit router_tc_split(const moe_config_t& c) {
+  const int tiles = router_tc_tiles(c);
+  const int num_kb = (c.d + 63) / 64;
+  int want = kRouterTcMaxBlocks / tiles;
+  if (want < 1) want = 1;
+  if (want > num_kb) want = num_kb;
+  const int per = (num_kb + want - 1) / want;
+  return RouterSplit{(num_kb + per - 1) / per, per};
+}
+// Probability partials the router writes: one per CTA, or one per tile when split.
+inline int router_tc_nparts(const moe_config_t& c) {
+  return router_tc_split(c).ksplit > 1 ? router_tc_tiles(c) : router_tc_grid(c);
+}
 
 inline int disp_blocks(const moe_config_t& c) {
   int64_t s = (int64_t)c.T * c.k;
@@ -66,7 +84,7 @@ inline int disp_blocks(const moe_config_t& c) {
 // Workspace regions (byte offsets, 256-aligned). Computed identically by the
 // size query and by every call.
 struct WsLayout {
-  size_t hdr, router_partial, router_tile_hist, disp_hist, disp_base, ffn_h, ffn_sched;
+  size_t hdr, router_partial, router_tile_hist, router_split, disp_hist, disp_base, ffn_h, ffn_sched;
   // fused layer intermediates
   size_t logits, topk_idx, topk_gate, slot_of, count, offset, token_of_row, xd, Y,
       prob_sum, f, P, L, dropped;
@@ -86,8 +104,8 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const void* Wg,
 bool router_tc_supported(const moe_config_t& c);
 cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                              const float* bias, const float* noise, float* logits, int32_t* idx,
-                             float* gate, float* partial, int32_t* tile_hist, int32_t* hdr,
-                             cudaStream_t s);
+                             float* gate, float* partial, int32_t* tile_hist, float* split_part,
+                             int32_t* hdr, cudaStream_t s);
 cudaError_t launch_prob_reduce(const moe_config_t& c, const float* partial, int nparts,
                                float* prob_sum, cudaStream_t s);
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,

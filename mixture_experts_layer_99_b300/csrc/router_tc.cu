@@ -14,6 +14,10 @@
 //   warp 0      TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
 //   warp 1      TMEM owner, MMA issuer
 //   warps 2-5   epilogue: one thread per token
+// When the batch has fewer 128-token tiles than the GPU has SMs (e.g. a
+// decode step of 64 tokens), the K range is split over several CTAs per tile
+// (SPLIT): each writes its fp32 partial logits, and router_split_epilogue
+// sums them in a fixed order and runs the same per-token epilogue.
 #include "moe_internal.h"
 #include "tc_ptx.cuh"
 
@@ -39,6 +43,13 @@ struct RouterCfg {
 };
 
 template <int EP>
+struct EpiSmem {
+  float red[4][EP];
+  float part[EP];
+  int hist[EP];
+};
+
+template <int EP>
 struct RouterSmem {
   uint64_t full[RouterCfg<EP>::STAGES];
   uint64_t empty[RouterCfg<EP>::STAGES];
@@ -47,9 +58,7 @@ struct RouterSmem {
   uint64_t final_bar;
   uint32_t tmem_base;
   int abort_flag;
-  float red[4][EP];
-  float part[EP];
-  int hist[EP];
+  EpiSmem<EP> epi;
 };
 
 template <int EP>
@@ -82,14 +91,115 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[EP]) {
   }
 }
 
+// One token per thread (thread r of the 128 owns token tile*128 + r): keys,
+// softmax, top-k (descending, ties to the lower index), gates, and the
+// tile's per-expert selection counts and sums of p (fixed order).
 template <int EP>
+__device__ __forceinline__ void router_tile_epilogue(
+    float (&v)[EP], int tile, int r, int lane, int quarter, int etid,
+    const float* __restrict__ bias, const float* __restrict__ noise, float tau, int T, int E,
+    int k, float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
+    int32_t* __restrict__ tile_hist, EpiSmem<EP>& es) {
+  for (int e = etid; e < EP; e += 128) es.hist[e] = 0;
+  const int t = tile * BM + r;
+  const bool valid = t < T;
+  // selection keys
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    float z = v[e];
+    if (e < E && valid) {
+      if (bias) z += __ldg(bias + e);
+      if (noise) z += __ldg(noise + (size_t)t * E + e);
+      z = z / tau;
+    }
+    v[e] = e < E ? z : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) m = fmaxf(m, v[e]);
+  if (valid && logits) {
+    float* lr = logits + (size_t)t * E;
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E) lr[e] = v[e];
+  }
+  // top-k on the keys: descending, ties to the lower index
+  uint64_t taken = 0;
+  float selv[kMaxK];
+  int seli[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    selv[j] = -INFINITY;
+    seli[j] = 0;
+    if (j < k) {
+      float bv = -INFINITY;
+      int bi = -1;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        const bool free_ = e < E && !((taken >> e) & 1ull);
+        if (free_ && (bi < 0 || v[e] > bv)) {
+          bv = v[e];
+          bi = e;
+        }
+      }
+      if (bi < 0) bi = 0;
+      taken |= 1ull << bi;
+      selv[j] = bv;
+      seli[j] = bi;
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    v[e] = e < E ? expf(v[e] - m) : 0.f;
+    s += v[e];
+  }
+  __syncwarp();
+  epi_bar();  // hist zeroed
+  if (valid) {
+    float psel[kMaxK], psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        psel[j] = expf(selv[j] - m) / s;
+        psum += psel[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k) {
+        idx[(size_t)t * k + j] = seli[j];
+        gate[(size_t)t * k + j] = psel[j] / psum;
+        atomicAdd(&es.hist[seli[j]], 1);
+      }
+    }
+  }
+  // per-expert sums of p over the tile's tokens: butterfly in each warp,
+  // then the 4 warps in a fixed order
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    float pe = (valid && e < E) ? v[e] / s : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+    if (lane == 0) es.red[quarter][e] = pe;
+  }
+  epi_bar();
+  for (int e = etid; e < E; e += 128) {
+    es.part[e] += ((es.red[0][e] + es.red[1][e]) + es.red[2][e]) + es.red[3][e];
+    if (tile_hist) tile_hist[(size_t)tile * E + e] = es.hist[e];
+  }
+  epi_bar();
+}
+
+template <int EP, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const float* __restrict__ bias,
                      const float* __restrict__ noise, float tau, int T, int d, int E, int k,
                      float* __restrict__ logits, int32_t* __restrict__ idx,
                      float* __restrict__ gate, float* __restrict__ partial,
-                     int32_t* __restrict__ tile_hist, int32_t* __restrict__ hdr) {
+                     int32_t* __restrict__ tile_hist, int32_t* __restrict__ hdr, int ksplit,
+                     int kb_per_split, float* __restrict__ split_part) {
   using Cfg = RouterCfg<EP>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -121,12 +231,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&st.tmem_base, Cfg::TCOLS);
     tmem_relinquish();
   }
-  for (int e = tid; e < EP; e += NUM_THREADS) st.part[e] = 0.f;
+  for (int e = tid; e < EP; e += NUM_THREADS) st.epi.part[e] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = st.tmem_base;
+  // work unit u = (tile, split): K blocks [split * kb_per_split, ...) of the tile
   const int ntiles = (T + BM - 1) / BM;
+  const int nunits = ntiles * ksplit;
   const int num_kb = (d + BK - 1) / BK;
   volatile int* abort_flag = &st.abort_flag;
 
@@ -135,8 +247,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int tile = u / ksplit, split = u % ksplit;
+        const int kb0 = split * kb_per_split;
+        const int kb1 = min(num_kb, kb0 + kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, hdr, 11)) {
             ok = false;
             break;
@@ -171,14 +286,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int split = u % ksplit;
+        const int kb0 = split * kb_per_split;
+        const int kb1 = min(num_kb, kb0 + kb_per_split);
         if (!mbar_wait(&st.tmem_empty[acc], acc_phase ^ 1u, abort_flag, hdr, 12)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * EP);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&st.full[stage], phase, abort_flag, hdr, 13)) {
             ok = false;
             break;
@@ -189,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
+                      (kb > kb0 || kk > 0) ? 1u : 0u);
           umma_commit(&st.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -216,7 +334,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int etid = tid - 64;  // 0..127
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      const int tile = u / ksplit, split = u % ksplit;
       if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) break;
       tc_fence_after();
       float v[EP];
@@ -227,103 +346,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
-      for (int e = etid; e < EP; e += 128) st.hist[e] = 0;
-      const int t = tile * BM + r;
-      const bool valid = t < T;
-      // selection keys
+      if (SPLIT) {
+        const int t = tile * BM + r;
+        if (t < T) {
+          float* pr = split_part + ((size_t)split * T + t) * E;
 #pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        float z = v[e];
-        if (e < E && valid) {
-          if (bias) z += __ldg(bias + e);
-          if (noise) z += __ldg(noise + (size_t)t * E + e);
-          z = z / tau;
+          for (int e = 0; e < EP; ++e)
+            if (e < E) pr[e] = v[e];
         }
-        v[e] = e < E ? z : -INFINITY;
+      } else {
+        router_tile_epilogue<EP>(v, tile, r, lane, quarter, etid, bias, noise, tau, T, E, k,
+                                 logits, idx, gate, tile_hist, st.epi);
       }
-      float m = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) m = fmaxf(m, v[e]);
-      if (valid && logits) {
-        float* lr = logits + (size_t)t * E;
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-          if (e < E) lr[e] = v[e];
-      }
-      // top-k on the keys: descending, ties to the lower index
-      uint64_t taken = 0;
-      float selv[kMaxK];
-      int seli[kMaxK];
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        selv[j] = -INFINITY;
-        seli[j] = 0;
-        if (j < k) {
-          float bv = -INFINITY;
-          int bi = -1;
-#pragma unroll
-          for (int e = 0; e < EP; ++e) {
-            const bool free_ = e < E && !((taken >> e) & 1ull);
-            if (free_ && (bi < 0 || v[e] > bv)) {
-              bv = v[e];
-              bi = e;
-            }
-          }
-          if (bi < 0) bi = 0;
-          taken |= 1ull << bi;
-          selv[j] = bv;
-          seli[j] = bi;
-        }
-      }
-      float s = 0.f;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        v[e] = e < E ? expf(v[e] - m) : 0.f;
-        s += v[e];
-      }
-      __syncwarp();
-      epi_bar();  // hist zeroed
-      if (valid) {
-        float psel[kMaxK], psum = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          if (j < k) {
-            psel[j] = expf(selv[j] - m) / s;
-            psum += psel[j];
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-          if (j < k) {
-            idx[(size_t)t * k + j] = seli[j];
-            gate[(size_t)t * k + j] = psel[j] / psum;
-            atomicAdd(&st.hist[seli[j]], 1);
-          }
-        }
-      }
-      // per-expert sums of p over the tile's tokens: butterfly in each warp,
-      // then the 4 warps in a fixed order
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        float pe = (valid && e < E) ? v[e] / s : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
-        if (lane == 0) st.red[quarter][e] = pe;
-      }
-      epi_bar();
-      for (int e = etid; e < E; e += 128) {
-        st.part[e] += ((st.red[0][e] + st.red[1][e]) + st.red[2][e]) + st.red[3][e];
-        if (tile_hist) tile_hist[(size_t)tile * E + e] = st.hist[e];
-      }
-      epi_bar();
     }
-    for (int e = etid; e < E; e += 128) partial[(size_t)blockIdx.x * E + e] = st.part[e];
+    if (!SPLIT)
+      for (int e = etid; e < E; e += 128) partial[(size_t)blockIdx.x * E + e] = st.epi.part[e];
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TCOLS);
+}
+
+// Second pass of the split router: thread r of block `tile` sums the ksplit
+// fp32 partial logits of token tile*128 + r in split order, then runs the
+// per-token epilogue. One block per tile, so the probability partials are
+// per tile.
+template <int EP>
+__global__ void __launch_bounds__(128) router_split_epilogue(
+    const float* __restrict__ split_part, int ksplit, const float* __restrict__ bias,
+    const float* __restrict__ noise, float tau, int T, int E, int k,
+    float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
+    float* __restrict__ partial, int32_t* __restrict__ tile_hist) {
+  __shared__ EpiSmem<EP> es;
+  const int tid = threadIdx.x, lane = tid & 31, quarter = tid >> 5;
+  const int tile = blockIdx.x;
+  for (int e = tid; e < EP; e += 128) es.part[e] = 0.f;
+  const int t = tile * BM + tid;
+  float v[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) v[e] = 0.f;
+  if (t < T) {
+    for (int sp = 0; sp < ksplit; ++sp) {
+      const float* pr = split_part + ((size_t)sp * T + t) * E;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e < E) v[e] += pr[e];
+    }
+  }
+  __syncthreads();
+  router_tile_epilogue<EP>(v, tile, tid, lane, quarter, tid, bias, noise, tau, T, E, k, logits,
+                           idx, gate, tile_hist, es);
+  for (int e = tid; e < E; e += 128) partial[(size_t)tile * E + e] = es.part[e];
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -357,26 +432,48 @@ bool map_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EP>
-cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
-                      const float* noise, float* logits, int32_t* idx, float* gate,
-                      float* partial, int32_t* tile_hist, int32_t* hdr, cudaStream_t s) {
+template <int EP, bool SPLIT>
+cudaError_t set_smem_attr() {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(router_tc_kernel<EP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(router_tc_kernel<EP, SPLIT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)router_smem_bytes<EP>());
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  return cudaSuccess;
+}
+
+template <int EP>
+cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
+                      const float* noise, float* logits, int32_t* idx, float* gate,
+                      float* partial, int32_t* tile_hist, float* split_part, int32_t* hdr,
+                      cudaStream_t s) {
   CUtensorMap mx, mw;
   if (!map_rows(&mx, x, c.d, c.T, BM) || !map_rows(&mw, Wg, c.d, c.E, EP))
     return cudaErrorInvalidValue;
-  router_tc_kernel<EP><<<router_tc_grid(c), NUM_THREADS, router_smem_bytes<EP>(), s>>>(
+  const RouterSplit sp = router_tc_split(c);
+  cudaError_t e;
+  if (sp.ksplit == 1) {
+    if ((e = set_smem_attr<EP, false>()) != cudaSuccess) return e;
+    router_tc_kernel<EP, false><<<router_tc_grid(c), NUM_THREADS, router_smem_bytes<EP>(), s>>>(
+        mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist,
+        hdr, 1, sp.kb_per_split, nullptr);
+    return cudaGetLastError();
+  }
+  if ((e = set_smem_attr<EP, true>()) != cudaSuccess) return e;
+  const int units = router_tc_tiles(c) * sp.ksplit;
+  router_tc_kernel<EP, true><<<units, NUM_THREADS, router_smem_bytes<EP>(), s>>>(
       mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist,
-      hdr);
+      hdr, sp.ksplit, sp.kb_per_split, split_part);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  router_split_epilogue<EP><<<router_tc_tiles(c), 128, 0, s>>>(
+      split_part, sp.ksplit, bias, noise, c.tau, c.T, c.E, c.k, logits, idx, gate, partial,
+      tile_hist);
   return cudaGetLastError();
 }
 
@@ -386,16 +483,21 @@ bool router_tc_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && 
 
 cudaError_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                              const float* bias, const float* noise, float* logits, int32_t* idx,
-                             float* gate, float* partial, int32_t* tile_hist, int32_t* hdr,
-                             cudaStream_t s) {
+                             float* gate, float* partial, int32_t* tile_hist, float* split_part,
+                             int32_t* hdr, cudaStream_t s) {
   const int ep = (c.E + 15) / 16 * 16;
+#define MOE_EP_CASE(EPV)                                                                       \
+  case EPV:                                                                                    \
+    return launch_ep<EPV>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist,        \
+                          split_part, hdr, s)
   switch (ep) {
-    case 16: return launch_ep<16>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
-    case 32: return launch_ep<32>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
-    case 48: return launch_ep<48>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
-    case 64: return launch_ep<64>(c, x, Wg, bias, noise, logits, idx, gate, partial, tile_hist, hdr, s);
+    MOE_EP_CASE(16);
+    MOE_EP_CASE(32);
+    MOE_EP_CASE(48);
+    MOE_EP_CASE(64);
     default: return cudaErrorInvalidValue;
   }
+#undef MOE_EP_CASE
 }
 
 }  // namespace moe
