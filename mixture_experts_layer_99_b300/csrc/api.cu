@@ -287,16 +287,15 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
     e = run_router(c, x, in->Wg, in->bias, in->noise, logits, idx, gate, ws, L, &rgrid, s);
   if (e == cudaSuccess) e = mark(1);
   // tensor-core router (bf16, E <= 64): its per-tile histograms and
-  // probability partials feed one scan + statistics kernel and a per-tile
-  // position kernel; for k = 1 GEMM2 writes the gated rows straight into y.
+  // probability partials feed one dispatch + statistics kernel (one block per
+  // tile); for k = 1 GEMM2 writes the gated rows straight into y.
   const bool fused_stats = router_tc_supported(c);
   const bool scatter = fused_stats && c.k == 1;
   if (e == cudaSuccess) {
     if (fused_stats) {
       e = launch_dispatch_from_router(c, idx, at<int32_t>(ws, L.router_tile_hist), partial,
-                                      rgrid, at<int32_t>(ws, L.disp_base), count, offset,
-                                      slot_of, token_of_row, prob_sum, f, P, Lb, dropped,
-                                      scatter ? y : nullptr, s);
+                                      rgrid, count, offset, slot_of, token_of_row, prob_sum, f,
+                                      P, Lb, dropped, scatter ? y : nullptr, s);
       if (e == cudaSuccess) e = launch_gather(c, x, token_of_row, offset, at<void>(ws, L.xd), R, s);
     } else {
       e = launch_dispatch(c, idx, x, count, offset, slot_of, token_of_row, at<void>(ws, L.xd),
@@ -370,12 +369,11 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const moe_layer
 int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
   // tensor-core router path: router (two kernels when its K range is split),
-  // scan + statistics, assign, gather, GEMM1, GEMM2, and the combine unless
-  // k = 1 (then GEMM2 writes y). FMA
-  // router path: router, dispatch (count, scan, assign, gather), GEMM1, GEMM2,
-  // combine, probability reduction, statistics.
+  // dispatch + statistics, gather, GEMM1, GEMM2, and the combine unless k = 1
+  // (then GEMM2 writes y). FMA router path: router, dispatch (count, scan,
+  // assign, gather), GEMM1, GEMM2, combine, probability reduction, statistics.
   if (router_tc_supported(*cfg))
-    return (cfg->k == 1 ? 6 : 7) + (router_tc_split(*cfg).ksplit > 1 ? 1 : 0);
+    return (cfg->k == 1 ? 5 : 6) + (router_tc_split(*cfg).ksplit > 1 ? 1 : 0);
   return 10;
 }
 

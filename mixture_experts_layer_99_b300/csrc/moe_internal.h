@@ -116,11 +116,10 @@ cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* t
                           const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s);
 cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* idx,
                                         const int32_t* tile_hist, const float* partial,
-                                        int nparts, int32_t* base, int32_t* count,
-                                        int32_t* offset, int32_t* slot_of,
-                                        int32_t* token_of_row, float* prob_sum, float* f,
-                                        float* P, float* Lb, int32_t* dropped, void* zero_y,
-                                        cudaStream_t s);
+                                        int nparts, int32_t* count, int32_t* offset,
+                                        int32_t* slot_of, int32_t* token_of_row,
+                                        float* prob_sum, float* f, float* P, float* Lb,
+                                        int32_t* dropped, void* zero_y, cudaStream_t s);
 cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
                        const void* W1, const void* W3, const void* W2, const void* b1,
                        const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,

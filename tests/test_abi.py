@@ -124,13 +124,13 @@ def test_workspace_checks():
 
 
 def test_launch_count_matches_path():
-    """Kernels per moe_layer_forward: 6 (tensor-core router, k = 1: GEMM2
-    writes y), 7 (tensor-core router, k > 1), +1 when the router's K range is
+    """Kernels per moe_layer_forward: 5 (tensor-core router, k = 1: GEMM2
+    writes y), 6 (tensor-core router, k > 1), +1 when the router's K range is
     split (fewer 128-token tiles than 148), 10 (fp32 or E > 64)."""
     from mixture_experts_layer_99_b300 import workloads as W
     L = moe.lib()
-    cases = [(W.WORKLOADS["switch_top1"], 7), (W.WORKLOADS["longtail"], 7),
-             (W.WORKLOADS["mixtral"], 7), (W.WORKLOADS["decode"], 8),
+    cases = [(W.WORKLOADS["switch_top1"], 6), (W.WORKLOADS["longtail"], 6),
+             (W.WORKLOADS["mixtral"], 6), (W.WORKLOADS["decode"], 7),
              (W.WORKLOADS["ref_fp32"], 10),
              (W.small(W.WORKLOADS["switch_top1"], T=64, d=64, H=64, E=128, k=2), 10)]
     for w, want in cases:
