@@ -48,6 +48,21 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def max_over_ranks(v: float, pg, device) -> float:
+    """The maximum of a per-rank value over all ranks (the value itself
+    without a process group). Used for step times only."""
+    if pg is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(w, rank: int, i: int) -> int:
+    """Seed of input set i on a rank: every rank draws its own batch."""
+    return w.seed + 1000 * rank + i
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -255,12 +270,12 @@ def main():
     peaks = load_peaks()
 
     # ---- inputs: rotating sets, different seed per rank and per set
-    base = W.make_inputs(w, seed=w.seed + 1000 * rank)
+    base = W.make_inputs(w, seed=rank_seed(w, rank, 0))
     fp = footprint_bytes(base)
     nsets = max(2, math.ceil(3 * L2_BYTES / fp))
     sets = [W.to_device(base, dev)]
     for i in range(1, nsets):
-        sets.append(W.to_device(W.make_inputs(w, seed=w.seed + 1000 * rank + i), dev))
+        sets.append(W.to_device(W.make_inputs(w, seed=rank_seed(w, rank, i)), dev))
     cfg = moe.config_from_workload(w)
     ws = moe.workspace(cfg, dev, host_io=True)
     out = moe.alloc_outputs(cfg, dev, full=True)
@@ -313,10 +328,7 @@ def main():
         pg.barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
     clk = clocks.stop() if clocks else None
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, pg, dev)
     value = w.T * world / (ms / 1e3)
     # the same K steps as direct (eager) calls, for comparison
     ev0.record(stream)
@@ -343,27 +355,40 @@ def main():
           for j, n in enumerate(names)}
     st["layer"] = sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(prof_steps)) / prof_steps
 
-    # ---- end to end through the host-buffer C call (pinned host x and y)
+    # ---- end to end through the host-buffer C call (pinned host x and y):
+    # every step copies its tokens in, runs the layer and copies y (and
+    # L_balance) out; steps alternate between two streams, each with its own
+    # workspace and output buffer, so one step's copies overlap the other's
+    # compute, as a serving loop would run them
+    e2e_streams = [stream, torch.cuda.Stream(dev)]
+    e2e_ws = [ws, moe.workspace(cfg, dev, host_io=True)]
     xh = [s["x"].cpu().pin_memory() for s in sets[:2]]
-    yh = torch.empty_like(xh[0]).pin_memory()
-    Lh = torch.empty(1, dtype=torch.float32).pin_memory()
+    yh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
+    Lh = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(10, min(args.steps, 500))
-    for i in range(3):
-        moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh, ws=ws, L_host=Lh)
+
+    def e2e_step(i):
+        j = i % 2
+        with torch.cuda.stream(e2e_streams[j]):
+            moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh[j], ws=e2e_ws[j],
+                                   L_host=Lh[j])
+
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(e2e_streams[0])
+    e2e_streams[1].wait_event(a)
     for i in range(e2e_steps):
-        moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh, ws=ws, L_host=Lh)
-    b.record(stream)
+        e2e_step(i)
+    done1 = torch.cuda.Event()
+    done1.record(e2e_streams[1])
+    e2e_streams[0].wait_event(done1)
+    b.record(e2e_streams[0])
     torch.cuda.synchronize(dev)
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, pg, dev)
     bytes_x = cfg.T * cfg.d * sets[0]["x"].element_size()
 
     # ---- roofline of the dominant kernel (the grouped GEMM, two launches per call)
@@ -407,7 +432,8 @@ def main():
             roofline=roof,
             cpu_baseline=cpu,
             e2e=dict(value=w.T * world / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=bytes_x,
-                     d2h_bytes_per_step=bytes_x + 4),
+                     d2h_bytes_per_step=bytes_x + 4, ms_per_step=e2e_ms,
+                     call="moe_layer_forward_host, steps alternating over two streams"),
             gpu_launches=moe.lib().moe_layer_forward_launch_count(moe.ctypes.byref(cfg))
             * args.steps,
             clocks=clk,

@@ -65,7 +65,13 @@ struct SmemTail {
   int tbase[kMaxE + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + sizeof(SmemTail);
+// Epilogue staging: each epilogue warp writes its 32 rows x 32 columns of
+// bf16 output (2 KB) here and stores it with one TMA bulk tensor store, so
+// global writes are whole 64-byte row segments instead of 16-byte pieces of
+// 32 different rows.
+constexpr int STAGE_OUT_BYTES = 32 * 32 * 2;
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) +
+                              EPI_WARPS * STAGE_OUT_BYTES + sizeof(SmemTail);
 
 // GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
@@ -119,6 +125,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB3,
+                           const __grid_constant__ CUtensorMap tmOut,
                            const int32_t* __restrict__ offset, int E, int N, int K,
                            const __nv_bfloat16* __restrict__ bias,
                            __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
@@ -130,7 +137,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * (A_BYTES + B_BYTES));
+  uint8_t* sOut = smem + STAGES * (A_BYTES + B_BYTES);
+  SmemTail& st = *reinterpret_cast<SmemTail*>(sOut + EPI_WARPS * STAGE_OUT_BYTES);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -303,25 +311,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         oscale = row_ok ? __ldg(o_scale + orow_idx) : 0.f;
       }
       __nv_bfloat16* orow = out + (size_t)orow_idx * N;
-      constexpr int CHUNKS = (MODE == kSwiglu ? 64 : 128) / 32;
-#pragma unroll 1
-      for (int ch = 0; ch < CHUNKS; ++ch) {
-        const int c = (MODE == kSwiglu ? 64 : 128) * half + 32 * ch;  // tile-local out column
-        uint32_t r[32];
+      // all 32 rows of this warp belong to the tile's expert: one TMA store
+      // per 32 columns; otherwise (the expert's last, partial tile, or the
+      // row scatter) direct stores of the valid rows
+      const bool warp_full = !SCATTER && (ti.m0 + quarter * 32 + 32 <= ti.mend);
+      uint8_t* my_out = sOut + ew * STAGE_OUT_BYTES;
+      // The warp's whole slice of the accumulator (128 fp32 columns, or 64
+      // gate + 64 up columns for SwiGLU) goes to registers with one wait, and
+      // the TMEM buffer is handed back to the MMA before the activation and
+      // the stores.
+      constexpr int OUTC = MODE == kSwiglu ? 64 : 128;  // output columns per warp
+      const int cbase = OUTC * half;                     // tile-local first column
+      uint32_t r[128];
+      if (MODE == kSwiglu) {
+        tmem_ld32(t_row + (uint32_t)cbase, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(t_row + (uint32_t)(cbase + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld32(t_row + (uint32_t)(128 + cbase), *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+        tmem_ld32(t_row + (uint32_t)(128 + cbase + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+          tmem_ld32(t_row + (uint32_t)(cbase + 32 * ch), *reinterpret_cast<uint32_t(*)[32]>(&r[32 * ch]));
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&st.tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+#pragma unroll
+      for (int ch = 0; ch < OUTC / 32; ++ch) {
+        const int c = cbase + 32 * ch;
         float v[32];
         if (MODE == kSwiglu) {
-          uint32_t u[32];
-          tmem_ld32(t_row + (uint32_t)c, r);
-          tmem_ld32(t_row + (uint32_t)(128 + c), u);
-          tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            v[j] = silu_f(__uint_as_float(r[j])) * __uint_as_float(u[j]);
+            v[j] = silu_f(__uint_as_float(r[32 * ch + j])) * __uint_as_float(r[64 + 32 * ch + j]);
         } else {
-          tmem_ld32(t_row + (uint32_t)c, r);
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[32 * ch + j]);
           if (bias) {
             const __nv_bfloat16* be = bias + (size_t)ti.e * N + ti.n0 + c;
 #pragma unroll
@@ -337,30 +366,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= oscale;
         }
-        if (row_ok) {
+        uint4 pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk[q]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            h2[j] = __floats2bfloat162_rn(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
+        }
+        if (warp_full) {
+          // the previous store from this buffer must have read it
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = pk[q];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, my_out, ti.n0 + c, ti.m0 + quarter * 32);
+            bulk_commit();
+          }
+        } else if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int col = ti.n0 + c + 8 * q;
-            if (col + 8 <= N) {
-              uint4 pk;
-              __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                h2[j] = __floats2bfloat162_rn(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
-              *reinterpret_cast<uint4*>(orow + col) = pk;
-            }
+            if (col + 8 <= N) *reinterpret_cast<uint4*>(orow + col) = pk[q];
           }
         }
-      }
-      tc_fence_before();
-      mbar_arrive(&st.tmem_empty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
       }
     }
   }
 
+  if (warp >= 2 && lane == 0) bulk_wait0();  // the epilogue's TMA stores are complete
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -414,8 +452,23 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint6
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 [rows, N] row-major, box [32 rows, 32 cols], no swizzle: the
+// epilogue's output blocks.
+bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t gdim[2] = {N, rows};
+  cuuint64_t gstride[1] = {N * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE, bool SCATTER>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                        const CUtensorMap& o,
                         const int32_t* offset, int E, int N, int K, const void* bias, void* out,
                         int64_t rows_bound, int32_t* hdr, const int32_t* o_rows,
                         const float* o_scale, cudaStream_t s) {
@@ -434,7 +487,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   const int sms = device_sm_count();
   const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
   grouped_gemm_tc_kernel<MODE, SCATTER><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
-      a, b, b3, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
+      a, b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
       static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale);
   return cudaGetLastError();
 }
@@ -445,10 +498,13 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
                           const void* W1, const void* W3, const void* W2, const void* b1,
                           const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
                           cudaStream_t s, const FfnFusion* fz) {
-  CUtensorMap mx, mh, mw1, mw3, mw2;
+  CUtensorMap mx, mh, mw1, mw3, mw2, moh, moy;
   const uint64_t R = (uint64_t)rows_bound;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   const bool scatter = fz && fz->scatter_rows;
+  // the scatter variant stores rows directly; its map is a placeholder
+  if (!make_map_out(&moh, h, c.H, R) || !make_map_out(&moy, scatter ? h : Y, scatter ? c.H : c.d, R))
+    return cudaErrorInvalidValue;
   if (!make_map_2d(&mx, xd, c.d, R) || !make_map_2d(&mh, h, c.H, R) ||
       !make_map_3d(&mw1, W1, c.d, c.H, c.E, swiglu ? 128 : UMMA_N) ||
       !make_map_3d(&mw2, W2, c.H, c.d, c.E, UMMA_N))
@@ -457,19 +513,19 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
   if (!swiglu) mw3 = mw1;
   cudaError_t e;
   if (swiglu)
-    e = launch_gemm<kSwiglu, false>(mx, mw1, mw3, offset, c.E, c.H, c.d, nullptr, h, rows_bound,
-                                    hdr, nullptr, nullptr, s);
+    e = launch_gemm<kSwiglu, false>(mx, mw1, mw3, moh, offset, c.E, c.H, c.d, nullptr, h,
+                                    rows_bound, hdr, nullptr, nullptr, s);
   else
-    e = launch_gemm<kGelu, false>(mx, mw1, mw3, offset, c.E, c.H, c.d, b1, h, rows_bound, hdr,
-                                  nullptr, nullptr, s);
+    e = launch_gemm<kGelu, false>(mx, mw1, mw3, moh, offset, c.E, c.H, c.d, b1, h, rows_bound,
+                                  hdr, nullptr, nullptr, s);
   if (e != cudaSuccess) return e;
   if (fz && fz->between && (e = cudaEventRecord(fz->between, s)) != cudaSuccess) return e;
   const void* b2e = swiglu ? nullptr : b2;
   if (scatter)
-    return launch_gemm<kPlain, true>(mh, mw2, mw2, offset, c.E, c.d, c.H, b2e, fz->y, rows_bound,
-                                     hdr, fz->scatter_rows, fz->scatter_scale, s);
-  return launch_gemm<kPlain, false>(mh, mw2, mw2, offset, c.E, c.d, c.H, b2e, Y, rows_bound, hdr,
-                                    nullptr, nullptr, s);
+    return launch_gemm<kPlain, true>(mh, mw2, mw2, moy, offset, c.E, c.d, c.H, b2e, fz->y,
+                                     rows_bound, hdr, fz->scatter_rows, fz->scatter_scale, s);
+  return launch_gemm<kPlain, false>(mh, mw2, mw2, moy, offset, c.E, c.d, c.H, b2e, Y, rows_bound,
+                                    hdr, nullptr, nullptr, s);
 }
 
 }  // namespace moe
