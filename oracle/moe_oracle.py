@@ -41,6 +41,10 @@ notes of the repository):
   uniform routing gives L_balance = 1, as [MoE-math] 2.2 states.
 * A token whose k slots are all dropped gets y = 0 (the layer adds no residual).
 * GELU is the exact erf form; SwiGLU is W2 (silu(W1 x) * (W3 x)), no biases.
+* A shared expert (the lpnh.cn guide, section 4.10, routes out-of-distribution
+  tokens to one) is read as an expert of the same FFN form that every token
+  passes through with weight 1, added to the routed sum and untouched by
+  capacity and drops.
 
 Parity status of each function is stated in its docstring; all are pinned by
 the CPU tests in ``tests/test_oracle.py``.
@@ -275,8 +279,16 @@ def route_from_logits(l, k: int, C: int):
     return dict(logits=l, p=p, ids=ids, gates=g, **disp, **aux)
 
 
+def shared_expert_rows(xr, shared: dict, act: str):
+    """The shared expert on rows xr: the same FFN form as a routed expert
+    (weights W1 [Hs, d], W3 [Hs, d] for SwiGLU, W2 [d, Hs], optional b1, b2
+    for GELU), applied to every token with weight 1."""
+    return expert_ffn_rows(xr, shared["W1"], shared["W2"], shared.get("W3"),
+                           shared.get("b1"), shared.get("b2"), act)
+
+
 def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
-                tokens=None, logits=None):
+                tokens=None, logits=None, shared=None):
     """The layer: router -> softmax -> top-k -> gates -> dispatch -> experts ->
     combine -> aux statistics.
 
@@ -285,6 +297,8 @@ def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
     otherwise the oracle's own fp64 logits are used.
     ``tokens``: if given, y is computed only for those tokens (routing is
     always computed for the whole batch, since capacity couples tokens).
+    ``shared``: optional shared-expert weights (see shared_expert_rows),
+    added with weight 1 to every token's output.
     Returns the routing dict plus y [len(tokens) or T, d]."""
     x = inp["x"]
     T = x.shape[0]
@@ -300,4 +314,6 @@ def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
     r["y"] = combine_tokens(tok, x, r["ids"], r["gates"], r["slot_of"],
                             inp["W1"], inp["W2"], inp.get("W3"), inp.get("b1"),
                             inp.get("b2"), act)
+    if shared is not None:
+        r["y"] = r["y"] + shared_expert_rows(as_f64(x[tok]), shared, act)
     return r

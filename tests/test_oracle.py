@@ -363,6 +363,47 @@ def pin_router_logits(o):
     np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-14)
 
 
+def _shared(rng, d, Hs, act):
+    W1 = rng.standard_normal((Hs, d)) / math.sqrt(d)
+    W3 = rng.standard_normal((Hs, d)) / math.sqrt(d) if act == "swiglu" else None
+    W2 = rng.standard_normal((d, Hs)) / math.sqrt(Hs)
+    b1 = rng.standard_normal(Hs) * 0.1 if act == "gelu" else None
+    b2 = rng.standard_normal(d) * 0.1 if act == "gelu" else None
+    return dict(W1=W1, W3=W3, W2=W2, b1=b1, b2=b2)
+
+
+def pin_shared_expert_alone(o):
+    """Routed experts with W2 = 0 (and no b2) contribute nothing, so the layer
+    is exactly the shared expert as a dense FFN."""
+    rng = _rng(12)
+    for act in ("gelu", "swiglu"):
+        T, d, H, Hs, E, k = 29, 10, 12, 18, 4, 2
+        x = rng.standard_normal((T, d))
+        W1, W3, W2, _, _ = _weights(rng, E, d, H, act == "swiglu", False)
+        inp = dict(x=x, Wg=rng.standard_normal((E, d)), W1=W1, W3=W3, W2=np.zeros_like(W2))
+        sh = _shared(rng, d, Hs, act)
+        r = o.moe_forward(inp, k=k, c=Fraction(1, 2), act=act, shared=sh)
+        want = _torch_ffn(x, sh["W1"], sh["W3"], sh["W2"], sh["b1"], sh["b2"], act)
+        np.testing.assert_allclose(r["y"], want, rtol=0, atol=1e-12)
+
+
+def pin_shared_expert_equal_to_single_routed(o):
+    """E = 1, k = 1, no drops and a shared expert with the routed expert's
+    weights: y = 2 FFN(x). Fully dropped tokens (C < T) keep the shared term."""
+    rng = _rng(13)
+    T, d, H = 21, 8, 14
+    x = rng.standard_normal((T, d))
+    W1, W3, W2, b1, b2 = _weights(rng, 1, d, H, False, True)
+    inp = dict(x=x, Wg=rng.standard_normal((1, d)), W1=W1, W2=W2, b1=b1, b2=b2)
+    sh = dict(W1=W1[0], W2=W2[0], b1=b1[0], b2=b2[0])
+    dense = _torch_ffn(x, W1[0], None, W2[0], b1[0], b2[0], "gelu")
+    r = o.moe_forward(inp, k=1, c=1, act="gelu", shared=sh)
+    np.testing.assert_allclose(r["y"], 2 * dense, rtol=0, atol=1e-12)
+    r = o.moe_forward(inp, k=1, c=Fraction(1, 3), act="gelu", shared=sh)   # C = 7
+    np.testing.assert_allclose(r["y"][:7], 2 * dense[:7], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(r["y"][7:], dense[7:], rtol=0, atol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -465,6 +506,14 @@ def _mutants():
         e = np.exp(np.asarray(l, float))
         return e / e.sum(axis=0, keepdims=True)
     m["softmax_wrong_axis"] = ("softmax", softmax_no_max_over_wrong_axis)
+
+    def shared_missing(xr, shared, act):
+        return 0.0 * o.__dict__["_orig_shared"](xr, shared, act)
+    m["shared_expert_dropped"] = ("shared_expert_rows", shared_missing)
+
+    def shared_halved(xr, shared, act):
+        return 0.5 * o.__dict__["_orig_shared"](xr, shared, act)
+    m["shared_expert_weight_half"] = ("shared_expert_rows", shared_halved)
     return m
 
 
@@ -476,7 +525,8 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     o = ORC
     originals = dict(_orig_topk=o.topk_ids, _orig_dispatch=o.dispatch,
                      _orig_aux=o.aux_stats, _orig_ffn=o.expert_ffn_rows,
-                     _orig_logits=o.router_logits, _orig_combine=o.combine_tokens)
+                     _orig_logits=o.router_logits, _orig_combine=o.combine_tokens,
+                     _orig_shared=o.shared_expert_rows)
     for k, v in originals.items():
         monkeypatch.setattr(o, k, v, raising=False)
     attr, bad = MUTANTS[name]
