@@ -57,16 +57,18 @@ inline int router_tc_grid(const moe_config_t& c) {
   const int t = router_tc_tiles(c);
   return t < kRouterTcMaxBlocks ? t : kRouterTcMaxBlocks;
 }
-// With fewer tiles than SMs the router splits each tile's K range (64-wide
-// blocks) over ksplit CTAs; ksplit * tiles <= 148 and every split is non-empty.
+// With very few tiles (a batch of at most 16 x 128 tokens) the router splits
+// each tile's K range (64-wide blocks) over up to 8 CTAs; every split is
+// non-empty. Larger batches keep one CTA per tile: measured on B300, the
+// second pass costs more than the split saves once there are 64 tiles.
 struct RouterSplit {
   int ksplit, kb_per_split;
 };
 inline RouterSplit router_tc_split(const moe_config_t& c) {
   const int tiles = router_tc_tiles(c);
   const int num_kb = (c.d + 63) / 64;
-  int want = kRouterTcMaxBlocks / tiles;
-  if (want < 1) want = 1;
+  if (tiles > 16) return RouterSplit{1, num_kb};
+  int want = 8;
   if (want > num_kb) want = num_kb;
   const int per = (num_kb + want - 1) / want;
   return RouterSplit{(num_kb + per - 1) / per, per};
@@ -91,9 +93,11 @@ struct WsLayout {
   // host-io staging
   size_t x_stage, y_stage;
   size_t total_core, total_layer, total_host;
+  // shared expert (after total_layer): one-group offsets, hidden rows, output rows
+  size_t sh_offset, sh_h, sh_y, total_shared;
 };
 
-WsLayout ws_layout(const moe_config_t& c, int num_sms);
+WsLayout ws_layout(const moe_config_t& c, int num_sms, int H_shared = 0);
 int device_sm_count();
 
 // ---- launchers (return cudaError_t of the launch) ----
@@ -141,7 +145,9 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
                           const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
                           cudaStream_t s, const FfnFusion* fz = nullptr);
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
-                           const float* gate, void* y, cudaStream_t s);
+                           const float* gate, void* y, cudaStream_t s,
+                           const void* base = nullptr);
+cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,
                        const float* partial, int nparts, float* f, float* P, float* L,
                        int32_t* dropped, cudaStream_t s);

@@ -126,10 +126,10 @@ def test_workspace_checks():
 def test_launch_count_matches_path():
     """Kernels per moe_layer_forward: 5 (tensor-core router, k = 1: GEMM2
     writes y), 6 (tensor-core router, k > 1), +1 when the router's K range is
-    split (fewer 128-token tiles than 148), 10 (fp32 or E > 64)."""
+    split (at most 16 tiles of 128 tokens), 10 (fp32 or E > 64)."""
     from mixture_experts_layer_99_b300 import workloads as W
     L = moe.lib()
-    cases = [(W.WORKLOADS["switch_top1"], 6), (W.WORKLOADS["longtail"], 6),
+    cases = [(W.WORKLOADS["switch_top1"], 5), (W.WORKLOADS["longtail"], 6),
              (W.WORKLOADS["mixtral"], 6), (W.WORKLOADS["decode"], 7),
              (W.WORKLOADS["ref_fp32"], 10),
              (W.small(W.WORKLOADS["switch_top1"], T=64, d=64, H=64, E=128, k=2), 10)]
@@ -138,3 +138,25 @@ def test_launch_count_matches_path():
         assert L.moe_layer_forward_launch_count(ctypes.byref(cfg)) == want, w.name
     bad = _cfg(T=0)
     assert L.moe_layer_forward_launch_count(ctypes.byref(bad)) == 0
+
+
+def test_shared_expert_validation():
+    L = moe.lib()
+    cfg = _cfg(act="swiglu")
+    r = ctypes.byref(cfg)
+    fake = 4096
+    inp = moe.LayerInputs(fake, fake, None, None, fake, fake, fake, None, None)
+    out = moe.LayerOutputs(*([fake] + [None] * 10))
+    ok = moe.SharedExpert(64, fake, fake, fake, None, None)
+    need = moe.c_size_t(0)
+    assert L.moe_workspace_size_shared(r, 64, ctypes.byref(need)) == 0
+    assert need.value > moe.workspace_size(cfg)
+    for bad in (moe.SharedExpert(0, fake, fake, fake, None, None),      # H = 0
+                moe.SharedExpert(60, fake, fake, fake, None, None),     # H not a multiple of 8
+                moe.SharedExpert(64, fake, None, fake, None, None),     # SwiGLU without W3
+                moe.SharedExpert(64, fake, fake, fake, fake, None)):    # bias with SwiGLU
+        assert L.moe_layer_forward_shared(r, ctypes.byref(inp), ctypes.byref(bad),
+                                          ctypes.byref(out), ctypes.c_void_p(4096),
+                                          need.value, None) == 1
+    assert L.moe_layer_forward_shared(r, ctypes.byref(inp), ctypes.byref(ok), ctypes.byref(out),
+                                      ctypes.c_void_p(4096), need.value - 1, None) == 3
