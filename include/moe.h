@@ -232,6 +232,33 @@ MOE_API moe_status_t moe_layer_forward(const moe_config_t *cfg, const moe_layer_
                                const moe_layer_outputs_t *out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* A shared expert: an expert of the layer's FFN form (act) that every token
+ * passes through with weight 1, its output added to the routed sum (the
+ * lpnh.cn guide, section 4.10, routes tokens to such an expert). It is not
+ * subject to capacity or drops. Weights [out, in] in the layer dtype. */
+typedef struct {
+  int32_t H;          /* hidden size of the shared expert (multiple of 8 bf16 / 4 fp32) */
+  const void *W1;     /* [H, d]                         */
+  const void *W3;     /* [H, d] for SwiGLU, else NULL   */
+  const void *W2;     /* [d, H]                         */
+  const void *b1;     /* [H] GELU only, may be NULL     */
+  const void *b2;     /* [d] GELU only, may be NULL     */
+} moe_shared_expert_t;
+
+/* Workspace bytes for moe_layer_forward_shared (the layer's plus the shared
+ * expert's hidden and output rows). */
+MOE_API moe_status_t moe_workspace_size_shared(const moe_config_t *cfg, int32_t H_shared,
+                                               size_t *bytes);
+
+/* moe_layer_forward plus a shared expert: y_t = E_shared(x_t) + sum over kept
+ * slots of g_j E_{K_j}(x_t). Same conventions and outputs as
+ * moe_layer_forward; ws must hold moe_workspace_size_shared bytes. */
+MOE_API moe_status_t moe_layer_forward_shared(const moe_config_t *cfg,
+                                              const moe_layer_inputs_t *in,
+                                              const moe_shared_expert_t *shared,
+                                              const moe_layer_outputs_t *out, void *ws,
+                                              size_t ws_bytes, moe_stream_t stream);
+
 /* moe_layer_forward with timing marks: stage_events points to six
  * cudaEvent_t handles (created by the caller, timing enabled) that are
  * recorded on `stream` before the router, after the router, after the

@@ -7,7 +7,7 @@
 
 namespace moe {
 
-WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
+WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/, int H_shared) {
   WsLayout L;
   memset(&L, 0, sizeof(L));
   const size_t s = elem_bytes(c);
@@ -51,6 +51,11 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/) {
   L.x_stage = take(T * (size_t)c.d * s);
   L.y_stage = take(T * (size_t)c.d * s);
   L.total_host = off;
+  off = L.total_layer;  // the shared expert's regions follow the layer's
+  L.sh_offset = take(8);
+  L.sh_h = take(T * (size_t)(H_shared > 0 ? H_shared : 1) * s);
+  L.sh_y = take(T * (size_t)c.d * s);
+  L.total_shared = off;
   return L;
 }
 
@@ -259,14 +264,17 @@ moe_status_t moe_aux_stats(const moe_config_t* cfg, const int32_t* expert_count,
 // ev (optional): six events recorded on s at the stage boundaries: before
 // the router, after the router, after the dispatch, after GEMM1, after GEMM2,
 // after the combine and statistics.
+// sh (optional): a shared expert; its output (rows of ws) is the base the
+// combine adds the routed slots to. ws must then follow ws_layout(c, 0, sh->H).
 static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
                                        const moe_layer_inputs_t* in,
                                        const moe_layer_outputs_t* out, void* y, float* Lout,
                                        void* ws, cudaStream_t s,
-                                       const cudaEvent_t* ev = nullptr) {
+                                       const cudaEvent_t* ev = nullptr,
+                                       const moe_shared_expert_t* sh = nullptr) {
   auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
   const moe_config_t& c = *cfg;
-  const WsLayout L = ws_layout(c, 0);
+  const WsLayout L = ws_layout(c, 0, sh ? sh->H : 0);
   int32_t* idx = out && out->topk_idx ? out->topk_idx : at<int32_t>(ws, L.topk_idx);
   float* gate = out && out->topk_gate ? out->topk_gate : at<float>(ws, L.topk_gate);
   int32_t* slot_of = out && out->slot_of ? out->slot_of : at<int32_t>(ws, L.slot_of);
@@ -290,7 +298,7 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
   // probability partials feed one dispatch + statistics kernel (one block per
   // tile); for k = 1 GEMM2 writes the gated rows straight into y.
   const bool fused_stats = router_tc_supported(c);
-  const bool scatter = fused_stats && c.k == 1;
+  const bool scatter = fused_stats && c.k == 1 && !sh;
   if (e == cudaSuccess) {
     if (fused_stats) {
       e = launch_dispatch_from_router(c, idx, at<int32_t>(ws, L.router_tile_hist), partial,
@@ -322,7 +330,23 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
     }
   }
   if (e == cudaSuccess) e = mark(4);
-  if (e == cudaSuccess && !scatter) e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s);
+  void* base = nullptr;
+  if (sh && e == cudaSuccess) {
+    // the shared expert: one group of all T token rows through the same FFN
+    moe_config_t cs = c;
+    cs.E = 1;
+    cs.k = 1;
+    cs.H = sh->H;
+    cs.capacity = c.T;
+    int32_t* soff = at<int32_t>(ws, L.sh_offset);
+    e = launch_one_group_offsets(soff, c.T, s);
+    if (e == cudaSuccess)
+      e = launch_ffn(cs, x, soff, sh->W1, sh->W3, sh->W2, sh->b1, sh->b2, at<void>(ws, L.sh_y),
+                     at<void>(ws, L.sh_h), c.T, at<int32_t>(ws, L.hdr), s);
+    base = at<void>(ws, L.sh_y);
+  }
+  if (e == cudaSuccess && !scatter)
+    e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s, base);
   if (!fused_stats) {
     if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
     if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
@@ -348,6 +372,39 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const moe_layer_inputs_t
   if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg, 0).total_layer)) != MOE_OK) return st;
   return layer_forward_impl(cfg, in->x, in, out, out->y, out->L_balance, ws,
                             (cudaStream_t)stream);
+}
+
+static moe_status_t check_shared(const moe_config_t* cfg, const moe_shared_expert_t* sh) {
+  if (!sh || !sh->W1 || !sh->W2) return MOE_ERR_INVALID_ARG;
+  const int align = cfg->dtype == MOE_F32 ? 4 : 8;
+  if (sh->H < 1 || sh->H % align) return MOE_ERR_INVALID_ARG;
+  if ((cfg->act == MOE_ACT_SWIGLU) != (sh->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (cfg->act == MOE_ACT_SWIGLU && (sh->b1 || sh->b2)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size_shared(const moe_config_t* cfg, int32_t H_shared,
+                                       size_t* bytes) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes || H_shared < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*cfg, 0, H_shared).total_shared;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward_shared(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                      const moe_shared_expert_t* shared,
+                                      const moe_layer_outputs_t* out, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if ((st = check_shared(cfg, shared)) != MOE_OK) return st;
+  if (!in->x || !out || !out->y) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg, 0, shared->H).total_shared)) != MOE_OK)
+    return st;
+  return layer_forward_impl(cfg, in->x, in, out, out->y, out->L_balance, ws,
+                            (cudaStream_t)stream, nullptr, shared);
 }
 
 moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const moe_layer_inputs_t* in,

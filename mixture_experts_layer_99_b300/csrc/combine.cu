@@ -43,11 +43,14 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
                     __float_as_uint(f[3]));
 }
 
+// base (optional, [T, d]): each token's sum starts from its base row (the
+// shared expert's output) instead of zero.
 template <typename T>
 __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y,
                                                      const int32_t* __restrict__ slot_of,
                                                      const float* __restrict__ gate, int T_,
-                                                     int k, int nvec, uint4* __restrict__ y) {
+                                                     int k, int nvec, uint4* __restrict__ y,
+                                                     const uint4* __restrict__ base) {
   constexpr int V = 16 / sizeof(T);
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T_) return;
@@ -63,6 +66,7 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (base) unpack(__ldg(base + (size_t)t * nvec + v), acc, (T*)nullptr);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (sl[j] < 0) continue;
@@ -123,16 +127,28 @@ __global__ void __launch_bounds__(NT) aux_kernel(const int32_t* __restrict__ cou
 }  // namespace
 
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
-                           const float* gate, void* y, cudaStream_t s) {
+                           const float* gate, void* y, cudaStream_t s, const void* base) {
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   const unsigned grid = (unsigned)((c.T + NW - 1) / NW);
+  const uint4* b = static_cast<const uint4*>(base);
   if (c.dtype == MOE_F32)
     combine_kernel<float><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of, gate,
-                                              c.T, c.k, nvec, static_cast<uint4*>(y));
+                                              c.T, c.k, nvec, static_cast<uint4*>(y), b);
   else
     combine_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of,
                                                       gate, c.T, c.k, nvec,
-                                                      static_cast<uint4*>(y));
+                                                      static_cast<uint4*>(y), b);
+  return cudaGetLastError();
+}
+
+// off[0] = 0, off[1] = rows: the one-group offsets of the shared expert.
+__global__ void one_group_offsets_kernel(int32_t* off, int rows) {
+  off[0] = 0;
+  off[1] = rows;
+}
+
+cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s) {
+  one_group_offsets_kernel<<<1, 1, 0, s>>>(off, rows);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,6 @@ constexpr int BM = 128;
 constexpr int BK = 64;       // one 128-byte swizzle row of bf16
 constexpr int UMMA_N = 256;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_WARPS = 8;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
@@ -52,6 +51,19 @@ constexpr int TMEM_COLS = 2 * UMMA_N;         // two accumulators
 
 enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2 };
 
+// Pipeline shapes, chosen per launch by the K extent (measured on B300):
+//   long K  (> 16 K blocks): 4 operand stages, 1 output staging buffer/warp;
+//   short K (<= 16 blocks, e.g. GEMM1 with d = 1024): 3 stages and 4 output
+//   buffers, so the epilogue's four stores per tile never wait on each other.
+template <int STAGES_, int OUT_BUFS_>
+struct Pipe {
+  static constexpr int STAGES = STAGES_;
+  static constexpr int OUT_BUFS = OUT_BUFS_;
+};
+using PipeLongK = Pipe<4, 1>;
+using PipeShortK = Pipe<3, 4>;
+
+template <int STAGES>
 struct SmemTail {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -70,8 +82,13 @@ struct SmemTail {
 // global writes are whole 64-byte row segments instead of 16-byte pieces of
 // 32 different rows.
 constexpr int STAGE_OUT_BYTES = 32 * 32 * 2;
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) +
-                              EPI_WARPS * STAGE_OUT_BYTES + sizeof(SmemTail);
+template <class PIPE>
+constexpr size_t smem_bytes() {
+  return 1024 /*align slack*/ + PIPE::STAGES * (A_BYTES + B_BYTES) +
+         EPI_WARPS * PIPE::OUT_BUFS * STAGE_OUT_BYTES + sizeof(SmemTail<PIPE::STAGES>);
+}
+static_assert(smem_bytes<PipeLongK>() <= 227 * 1024, "shared memory");
+static_assert(smem_bytes<PipeShortK>() <= 227 * 1024, "shared memory");
 
 // GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
@@ -101,7 +118,8 @@ struct TileInfo {
 };
 
 // tile -> (expert, first row, end row of the expert, first output column)
-__device__ __forceinline__ TileInfo tile_info(const SmemTail& st, int E, int n_tiles_n, int tile,
+template <class ST>
+__device__ __forceinline__ TileInfo tile_info(const ST& st, int E, int n_tiles_n, int tile,
                                               int bn_out) {
   int lo = 0, hi = E - 1;  // largest e with tbase[e] <= tile
   while (lo < hi) {
@@ -120,7 +138,7 @@ __device__ __forceinline__ TileInfo tile_info(const SmemTail& st, int E, int n_t
   return ti;
 }
 
-template <int MODE, bool SCATTER>
+template <int MODE, bool SCATTER, class PIPE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -132,13 +150,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            const int32_t* __restrict__ o_rows,
                            const float* __restrict__ o_scale) {
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
+  constexpr int STAGES = PIPE::STAGES;
+  constexpr int OUT_BUFS = PIPE::OUT_BUFS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   uint8_t* sOut = smem + STAGES * (A_BYTES + B_BYTES);
-  SmemTail& st = *reinterpret_cast<SmemTail*>(sOut + EPI_WARPS * STAGE_OUT_BYTES);
+  SmemTail<STAGES>& st =
+      *reinterpret_cast<SmemTail<STAGES>*>(sOut + EPI_WARPS * OUT_BUFS * STAGE_OUT_BYTES);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -297,6 +318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = ew >> 2;              // which half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
+    int n_stores = 0;  // TMA stores issued by this warp (buffer = n_stores % OUT_BUFS)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = tile_info(st, E, n_tiles_n, tile, BN_OUT);
       if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 4)) break;
@@ -315,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // per 32 columns; otherwise (the expert's last, partial tile, or the
       // row scatter) direct stores of the valid rows
       const bool warp_full = !SCATTER && (ti.m0 + quarter * 32 + 32 <= ti.mend);
-      uint8_t* my_out = sOut + ew * STAGE_OUT_BYTES;
+      uint8_t* my_out0 = sOut + ew * OUT_BUFS * STAGE_OUT_BYTES;
       // The warp's whole slice of the accumulator (128 fp32 columns, or 64
       // gate + 64 up columns for SwiGLU) goes to registers with one wait, and
       // the TMEM buffer is handed back to the MMA before the activation and
@@ -375,8 +397,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             h2[j] = __floats2bfloat162_rn(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
         }
         if (warp_full) {
-          // the previous store from this buffer must have read it
-          if (lane == 0) bulk_wait_read0();
+          // the store that last used this buffer (OUT_BUFS stores ago) must
+          // have read it
+          uint8_t* my_out = my_out0 + (n_stores % OUT_BUFS) * STAGE_OUT_BYTES;
+          ++n_stores;
+          if (lane == 0) {
+            if (OUT_BUFS == 1) bulk_wait_read0();
+            else bulk_wait_read<OUT_BUFS - 1>();
+          }
           __syncwarp();
           uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
 #pragma unroll
@@ -466,18 +494,18 @@ bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool SCATTER>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
-                        const CUtensorMap& o,
-                        const int32_t* offset, int E, int N, int K, const void* bias, void* out,
-                        int64_t rows_bound, int32_t* hdr, const int32_t* o_rows,
-                        const float* o_scale, cudaStream_t s) {
+template <int MODE, bool SCATTER, class PIPE>
+cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                          const CUtensorMap& o, const int32_t* offset, int E, int N, int K,
+                          const void* bias, void* out, int64_t rows_bound, int32_t* hdr,
+                          const int32_t* o_rows, const float* o_scale, cudaStream_t s) {
+  constexpr size_t SMEM_BYTES = smem_bytes<PIPE>();
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, SCATTER>,
+    e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, SCATTER, PIPE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -486,10 +514,22 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   const int64_t tiles_bound = ((rows_bound + BM - 1) / BM + E) * ((N + BN_OUT - 1) / BN_OUT);
   const int sms = device_sm_count();
   const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
-  grouped_gemm_tc_kernel<MODE, SCATTER><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
+  grouped_gemm_tc_kernel<MODE, SCATTER, PIPE><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
       a, b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
       static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale);
   return cudaGetLastError();
+}
+
+template <int MODE, bool SCATTER>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
+                        const CUtensorMap& o, const int32_t* offset, int E, int N, int K,
+                        const void* bias, void* out, int64_t rows_bound, int32_t* hdr,
+                        const int32_t* o_rows, const float* o_scale, cudaStream_t s) {
+  if ((K + BK - 1) / BK <= 16)
+    return launch_gemm_p<MODE, SCATTER, PipeShortK>(a, b, b3, o, offset, E, N, K, bias, out,
+                                                    rows_bound, hdr, o_rows, o_scale, s);
+  return launch_gemm_p<MODE, SCATTER, PipeLongK>(a, b, b3, o, offset, E, N, K, bias, out,
+                                                 rows_bound, hdr, o_rows, o_scale, s);
 }
 
 }  // namespace

@@ -390,9 +390,22 @@ __global__ void __launch_bounds__(128) router_split_epilogue(
   if (t < T) {
     for (int sp = 0; sp < ksplit; ++sp) {
       const float* pr = split_part + ((size_t)sp * T + t) * E;
+      if ((E & 3) == 0) {  // rows are 16-byte aligned: vector loads
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) v[e] += pr[e];
+        for (int e = 0; e < EP; e += 4) {
+          if (e < E) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(pr + e));
+            v[e] += q.x;
+            v[e + 1] += q.y;
+            v[e + 2] += q.z;
+            v[e + 3] += q.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+          if (e < E) v[e] += __ldg(pr + e);
+      }
     }
   }
   __syncthreads();

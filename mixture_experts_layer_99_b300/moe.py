@@ -29,7 +29,8 @@ EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspa
             "moe_workspace_size_host", "moe_workspace_init", "moe_device_status",
             "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
             "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
-            "moe_layer_forward_launch_count", "moe_layer_forward_profiled"]
+            "moe_layer_forward_launch_count", "moe_layer_forward_profiled",
+            "moe_workspace_size_shared", "moe_layer_forward_shared", "moe_dispatch_static_scratch"]
 
 
 class MoEError(RuntimeError):
@@ -53,6 +54,11 @@ class LayerInputs(ctypes.Structure):
     _fields_ = [("x", c_void_p), ("Wg", c_void_p), ("bias", c_void_p), ("noise", c_void_p),
                 ("W1", c_void_p), ("W3", c_void_p), ("W2", c_void_p), ("b1", c_void_p),
                 ("b2", c_void_p)]
+
+
+class SharedExpert(ctypes.Structure):
+    _fields_ = [("H", c_int32), ("W1", c_void_p), ("W3", c_void_p), ("W2", c_void_p),
+                ("b1", c_void_p), ("b2", c_void_p)]
 
 
 class LayerOutputs(ctypes.Structure):
@@ -92,6 +98,10 @@ def lib():
         "moe_layer_forward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs),
                                         vp, c_size_t, vp]),
         "moe_layer_forward_launch_count": (c_int32, [cfgp]),
+        "moe_workspace_size_shared": (c_int32, [cfgp, c_int32, POINTER(c_size_t)]),
+        "moe_layer_forward_shared": (c_int32, [cfgp, POINTER(LayerInputs),
+                                               POINTER(SharedExpert), POINTER(LayerOutputs),
+                                               vp, c_size_t, vp]),
         "moe_layer_forward_profiled": (c_int32, [cfgp, POINTER(LayerInputs),
                                                  POINTER(LayerOutputs), vp, c_size_t, vp,
                                                  POINTER(c_void_p)]),
@@ -322,6 +332,40 @@ def layer_forward(cfg, inp: dict, *, ws=None, out: Optional[dict] = None, full=T
     ws = workspace(cfg, dev) if ws is None else ws
     _call("moe_layer_forward", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(lo),
           _ptr(ws), ws.numel(), _stream(dev))
+    return out
+
+
+def workspace_shared(cfg: Config, H_shared: int, device="cuda") -> torch.Tensor:
+    n = c_size_t(0)
+    _call("moe_workspace_size_shared", ctypes.byref(cfg), H_shared, ctypes.byref(n))
+    ws = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n.value]
+    _call("moe_workspace_init", c_void_p(ws.data_ptr()), n.value,
+          c_void_p(_stream(ws.device)))
+    return ws
+
+
+def layer_forward_shared(cfg, inp: dict, shared: dict, *, ws=None, out=None, full=True):
+    """The fused layer plus a shared expert (every token, weight 1). ``shared``
+    holds W1 [Hs, d], W2 [d, Hs], and W3 [Hs, d] (SwiGLU) or optional b1 [Hs],
+    b2 [d] (GELU)."""
+    dev = inp["x"].device
+    dt = _dt(cfg)
+    li = _layer_inputs(cfg, inp, dev)
+    Hs = shared["W1"].shape[0]
+    _need(shared["W1"], "shared W1", dt, (Hs, cfg.d), dev)
+    _need(shared["W2"], "shared W2", dt, (cfg.d, Hs), dev)
+    _opt(shared.get("W3"), "shared W3", dt, (Hs, cfg.d), dev)
+    _opt(shared.get("b1"), "shared b1", dt, (Hs,), dev)
+    _opt(shared.get("b2"), "shared b2", dt, (cfg.d,), dev)
+    se = SharedExpert(Hs, _ptr(shared["W1"]), _ptr(shared.get("W3")), _ptr(shared["W2"]),
+                      _ptr(shared.get("b1")), _ptr(shared.get("b2")))
+    out = alloc_outputs(cfg, dev, full) if out is None else out
+    lo = LayerOutputs(*[_ptr(out.get(n)) for n, _ in LayerOutputs._fields_])
+    ws = workspace_shared(cfg, Hs, dev) if ws is None else ws
+    _call("moe_layer_forward_shared", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(se),
+          ctypes.byref(lo), _ptr(ws), ws.numel(), _stream(dev))
     return out
 
 

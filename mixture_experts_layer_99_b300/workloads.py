@@ -52,6 +52,7 @@ class Workload:
     noise: Optional[str] = None         # None or "gumbel"
     tau: float = 1.0
     seed: int = 0
+    shared_H: int = 0                   # > 0: a shared expert of this hidden size
 
     @property
     def torch_dtype(self):
@@ -81,6 +82,10 @@ WORKLOADS = {
                          router_bias="zipf", noise="gumbel", tau=1.0),
     "decode": Workload("decode", T=64, d=4096, E=64, k=2, H=1408,
                        act="swiglu", dtype="bf16", c=Fraction(32)),
+    # the long-tail layer plus one always-on shared expert of the same width
+    "longtail_shared": Workload("longtail_shared", T=32768, d=2048, E=64, k=2, H=1408,
+                                act="swiglu", dtype="bf16", c=Fraction(2),
+                                router_bias="zipf", noise="gumbel", tau=1.0, shared_H=1408),
 }
 
 
@@ -127,8 +132,17 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
         u = torch.rand(w.T, w.E, generator=gen, dtype=torch.float64)
         u = u.clamp_(1e-12, 1.0 - 1e-12)
         noise = (-torch.log(-torch.log(u))).to(torch.float32)
-    return dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, b1=b1, b2=b2, bias=bias,
-                noise=noise)
+    out = dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, b1=b1, b2=b2, bias=bias, noise=noise)
+    if w.shared_H > 0:   # drawn last, so the routed inputs do not change
+        Hs = w.shared_H
+        out["shared"] = dict(
+            W1=_randn(gen, (Hs, w.d), 1.0 / math.sqrt(w.d), dt),
+            W3=(_randn(gen, (Hs, w.d), 1.0 / math.sqrt(w.d), dt)
+                if w.act == "swiglu" else None),
+            W2=_randn(gen, (w.d, Hs), 1.0 / math.sqrt(Hs), dt),
+            b1=torch.zeros(Hs, dtype=dt) if w.expert_bias else None,
+            b2=torch.zeros(w.d, dtype=dt) if w.expert_bias else None)
+    return out
 
 
 def small(w: Workload, T: int, d: int, H: int, E: Optional[int] = None,
@@ -164,4 +178,10 @@ def make_rows(R: int, d: int, dtype, seed: int = 0):
 
 
 def to_device(inp: dict, device) -> dict:
-    return {k: (None if v is None else v.to(device).contiguous()) for k, v in inp.items()}
+    def mv(v):
+        if v is None:
+            return None
+        if isinstance(v, dict):
+            return to_device(v, device)
+        return v.to(device).contiguous()
+    return {k: mv(v) for k, v in inp.items()}

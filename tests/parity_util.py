@@ -52,7 +52,11 @@ def check_layer(w: W.Workload, device, n_sample=None, seed=None, inp=None):
     inp = W.make_inputs(w, seed) if inp is None else inp
     cfg = moe.config_from_workload(w)
     dinp = W.to_device(inp, device)
-    out = moe.layer_forward(cfg, dinp)
+    shared = inp.get("shared")
+    if shared is not None:
+        out = moe.layer_forward_shared(cfg, dinp, dinp["shared"])
+    else:
+        out = moe.layer_forward(cfg, dinp)
     torch.cuda.synchronize()
     C = ORC.capacity(w.c, w.k, w.T, w.E)
     assert cfg.capacity == C
@@ -76,12 +80,14 @@ def check_layer(w: W.Workload, device, n_sample=None, seed=None, inp=None):
     ref_y = ORC.combine_tokens(tokens, inp["x"], r["ids"], r["gates"], r["slot_of"],
                                inp["W1"], inp["W2"], inp.get("W3"), inp.get("b1"),
                                inp.get("b2"), w.act)
+    if shared is not None:
+        ref_y = ref_y + ORC.shared_expert_rows(ORC.as_f64(inp["x"][tokens]), shared, w.act)
     y = np_of(out["y"])[tokens]
     e_y = rel_err(y, ref_y)
     assert e_y <= TOL_Y[w.dtype], f"y rel err {e_y}"
-    # tokens with every slot dropped are exactly zero
+    # tokens with every slot dropped are exactly zero (without a shared expert)
     all_dropped = (r["slot_of"] < 0).all(axis=1)
-    if all_dropped.any():
+    if all_dropped.any() and shared is None:
         assert (out["y"][torch.from_numpy(all_dropped).to(device)] == 0).all()
     flips = int((ORC.topk_ids(ref_l, w.k) != r["ids"]).any(axis=1).sum())
     return dict(logits_err=e_l, y_err=e_y, dropped=r["dropped"], L=r["L"],

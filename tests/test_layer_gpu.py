@@ -114,3 +114,25 @@ def test_layer_profiled_matches_and_times(name):
     assert all(t >= 0 for t in times)
     assert evs[0].elapsed_time(evs[5]) > 0
 
+
+
+SHARED = {
+    "longtail_shared_small": W.small(WL["longtail_shared"], T=1500, d=128, H=192).with_(shared_H=256),
+    "switch_shared_small": W.small(WL["switch_top1"], T=900, d=256, H=512).with_(shared_H=384),
+    "ref_fp32_shared": WL["ref_fp32"].with_(shared_H=128),
+    "heavy_drops_shared": W.small(WL["longtail"], T=777, d=64, H=64,
+                                  c=Fraction(1, 4)).with_(shared_H=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHARED))
+def test_layer_shared_expert_small(name):
+    """moe_layer_forward_shared against the oracle with its shared expert:
+    every token, dropped or not, gets the shared FFN with weight 1."""
+    res = check_layer(SHARED[name], DEV)
+    assert res["tokens_checked"] == SHARED[name].T
+
+
+def test_layer_shared_expert_full_size():
+    res = check_layer(WL["longtail_shared"], DEV, n_sample=512)
+    print({k: v for k, v in res.items() if k not in ("out", "r")})
