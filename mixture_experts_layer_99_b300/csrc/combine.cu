@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y
                                                      int k, int nvec, uint4* __restrict__ y,
                                                      const uint4* __restrict__ base) {
   constexpr int V = 16 / sizeof(T);
+  pdl_wait();
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T_) return;
   const int lane = threadIdx.x & 31;
@@ -131,25 +132,24 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* 
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   const unsigned grid = (unsigned)((c.T + NW - 1) / NW);
   const uint4* b = static_cast<const uint4*>(base);
+  const uint4* Yv = static_cast<const uint4*>(Y);
+  uint4* yv = static_cast<uint4*>(y);
   if (c.dtype == MOE_F32)
-    combine_kernel<float><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of, gate,
-                                              c.T, c.k, nvec, static_cast<uint4*>(y), b);
-  else
-    combine_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(static_cast<const uint4*>(Y), slot_of,
-                                                      gate, c.T, c.k, nvec,
-                                                      static_cast<uint4*>(y), b);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<float>, dim3(grid), dim3(NT), 0, s, Yv, slot_of, gate, c.T,
+                      c.k, nvec, yv, b);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(NT), 0, s, Yv, slot_of,
+                    gate, c.T, c.k, nvec, yv, b);
 }
 
 // off[0] = 0, off[1] = rows: the one-group offsets of the shared expert.
 __global__ void one_group_offsets_kernel(int32_t* off, int rows) {
+  pdl_wait();
   off[0] = 0;
   off[1] = rows;
 }
 
 cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s) {
-  one_group_offsets_kernel<<<1, 1, 0, s>>>(off, rows);
-  return cudaGetLastError();
+  return launch_pdl(one_group_offsets_kernel, dim3(1), dim3(1), 0, s, off, rows);
 }
 
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,

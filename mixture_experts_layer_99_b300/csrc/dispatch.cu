@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(NT) disp_gather_kernel(const uint4* __restrict
                                                          const int32_t* __restrict__ offset,
                                                          int E, int nvec,
                                                          uint4* __restrict__ xd) {
+  pdl_wait();
   const int nrows = offset[E];
   const int row = blockIdx.x * NW + (threadIdx.x >> 5);
   if (row >= nrows) return;
@@ -158,11 +159,10 @@ cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* t
                           const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s) {
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   const int64_t gblk = (rows_bound + NW - 1) / NW;
-  if (gblk > 0)
-    disp_gather_kernel<<<(unsigned)gblk, NT, 0, s>>>(static_cast<const uint4*>(x),
-                                                     token_of_row, offset, c.E, nvec,
-                                                     static_cast<uint4*>(xd));
-  return cudaGetLastError();
+  if (gblk <= 0) return cudaSuccess;
+  return launch_pdl(disp_gather_kernel, dim3((unsigned)gblk), dim3(NT), 0, s,
+                    static_cast<const uint4*>(x), token_of_row, offset, c.E, nvec,
+                    static_cast<uint4*>(xd));
 }
 
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     base[e] = 0;
   }
   for (int i = tid; i < 8 * kMaxE; i += 256) (&wcnt[0][0])[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int nh = ntiles * E;
   for (int i = tid; i < nh; i += 256) {
@@ -181,11 +182,10 @@ cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* id
                                         int32_t* dropped, void* zero_y, cudaStream_t s) {
   const int ntiles = router_tc_tiles(c);
   const int y_vec16 = (int)((size_t)c.d * elem_bytes(c) / 16);
-  dispatch_tiles_kernel<<<ntiles, 256, 0, s>>>(
-      idx, c.T, c.k, c.E, c.capacity, tile_hist, ntiles, partial, nparts, count, offset,
-      slot_of, token_of_row, prob_sum, f, P, Lb, dropped,
-      c.k == 1 ? static_cast<uint4*>(zero_y) : nullptr, y_vec16);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_tiles_kernel, dim3(ntiles), dim3(256), 0, s, idx, c.T, c.k, c.E,
+                    c.capacity, tile_hist, ntiles, partial, nparts, count, offset, slot_of,
+                    token_of_row, prob_sum, f, P, Lb, dropped,
+                    c.k == 1 ? static_cast<uint4*>(zero_y) : (uint4*)nullptr, y_vec16);
 }
 
 }  // namespace moe

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(&st.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();
   for (int i = tid; i <= E; i += NUM_THREADS) st.off[i] = offset[i];
   __syncthreads();
   const int n_tiles_n = (N + BN_OUT - 1) / BN_OUT;
@@ -514,10 +515,10 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   const int64_t tiles_bound = ((rows_bound + BM - 1) / BM + E) * ((N + BN_OUT - 1) / BN_OUT);
   const int sms = device_sm_count();
   const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
-  grouped_gemm_tc_kernel<MODE, SCATTER, PIPE><<<grid > 0 ? grid : 1, NUM_THREADS, SMEM_BYTES, s>>>(
-      a, b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
-      static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_tc_kernel<MODE, SCATTER, PIPE>, dim3(grid > 0 ? grid : 1),
+                    dim3(NUM_THREADS), SMEM_BYTES, s, a, b, b3, o, offset, E, N, K,
+                    static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(out),
+                    hdr, o_rows, o_scale);
 }
 
 template <int MODE, bool SCATTER>

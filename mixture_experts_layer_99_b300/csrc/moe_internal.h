@@ -10,6 +10,34 @@
 
 namespace moe {
 
+// Programmatic dependent launch: the kernels of the layer are launched with
+// programmatic stream serialisation, so a kernel is scheduled as soon as every
+// CTA of its predecessor has exited and runs its prologue (mbarrier set-up,
+// TMEM allocation, tensor-map prefetch) while the predecessor's writes are
+// flushed. Each such kernel calls pdl_wait() before its first global-memory
+// access; it returns once the predecessor grid has completed and its writes
+// are visible. No kernel triggers its dependents early: letting them launch
+// at the start of the predecessor (griddepcontrol.launch_dependents) parked
+// their CTAs on the SMs the predecessor was still using and made the layer
+// slower.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 

@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
   const uint32_t tmem_base = st.tmem_base;
   // work unit u = (tile, split): K blocks [split * kb_per_split, ...) of the tile
   const int ntiles = (T + BM - 1) / BM;
@@ -383,6 +384,7 @@ __global__ void __launch_bounds__(128) router_split_epilogue(
   const int tid = threadIdx.x, lane = tid & 31, quarter = tid >> 5;
   const int tile = blockIdx.x;
   for (int e = tid; e < EP; e += 128) es.part[e] = 0.f;
+  pdl_wait();
   const int t = tile * BM + tid;
   float v[EP];
 #pragma unroll
@@ -473,21 +475,21 @@ cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, cons
   cudaError_t e;
   if (sp.ksplit == 1) {
     if ((e = set_smem_attr<EP, false>()) != cudaSuccess) return e;
-    router_tc_kernel<EP, false><<<router_tc_grid(c), NUM_THREADS, router_smem_bytes<EP>(), s>>>(
-        mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist,
-        hdr, 1, sp.kb_per_split, nullptr);
-    return cudaGetLastError();
+    return launch_pdl(router_tc_kernel<EP, false>, dim3(router_tc_grid(c)), dim3(NUM_THREADS),
+                      router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau, c.T, c.d, c.E,
+                      c.k, logits, idx, gate, partial, tile_hist, hdr, 1, sp.kb_per_split,
+                      (float*)nullptr);
   }
   if ((e = set_smem_attr<EP, true>()) != cudaSuccess) return e;
   const int units = router_tc_tiles(c) * sp.ksplit;
-  router_tc_kernel<EP, true><<<units, NUM_THREADS, router_smem_bytes<EP>(), s>>>(
-      mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist,
-      hdr, sp.ksplit, sp.kb_per_split, split_part);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  router_split_epilogue<EP><<<router_tc_tiles(c), 128, 0, s>>>(
-      split_part, sp.ksplit, bias, noise, c.tau, c.T, c.E, c.k, logits, idx, gate, partial,
-      tile_hist);
-  return cudaGetLastError();
+  e = launch_pdl(router_tc_kernel<EP, true>, dim3(units), dim3(NUM_THREADS),
+                 router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k,
+                 logits, idx, gate, partial, tile_hist, hdr, sp.ksplit, sp.kb_per_split,
+                 split_part);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(router_split_epilogue<EP>, dim3(router_tc_tiles(c)), dim3(128), 0, s,
+                    (const float*)split_part, sp.ksplit, bias, noise, c.tau, c.T, c.E, c.k,
+                    logits, idx, gate, partial, tile_hist);
 }
 
 }  // namespace
