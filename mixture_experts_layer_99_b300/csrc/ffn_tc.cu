@@ -92,22 +92,29 @@ static_assert(smem_bytes<PipeShortK>() <= 227 * 1024, "shared memory");
 
 // GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
-// formula 7.1.26 (Hastings): for z >= 0, erf(z) = 1 - q(z) with
-// q(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2), t = 1/(1 + p z),
-// |error| <= 1.5e-7. Written as GELU(u) = u - u q / 2 for u >= 0 and u q / 2
-// for u < 0, so there is neither a branch (all lanes of a warp take the same
-// path) nor a cancellation for negative u.
+// formula 7.1.26 (Hastings): for z >= 0, erfc(z) = 1 - erf(z) ~ q(z) with
+// q(z) = t (a1 + a2 t + a3 t^2 + a4 t^3 + a5 t^4) exp(-z^2), t = 1/(1 + p z),
+// |error| <= 1.5e-7. Since erf is odd, GELU(u) = max(u, 0) - |u| q(|u|/sqrt 2) / 2
+// for either sign of u: no branch and no cancellation for negative u.
+// With s = z sqrt(log2 e) the exponential is 2^(-s^2) (one ex2) and p z =
+// (p / sqrt(log2 e)) s, so z itself is never formed.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float gelu_as(float u) {
-  const float z = fabsf(u) * 0.70710678118654752f;
-  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+  constexpr float kS = 0.84932180028801904f;    // sqrt(log2 e) / sqrt 2
+  constexpr float kP = 0.27273748087922250f;    // p / sqrt(log2 e), p = 0.3275911
+  const float s = fabsf(u) * kS;
+  const float t = __fdividef(1.f, fmaf(kP, s, 1.f));
+  const float e = ex2_approx(-s * s);
   float poly = fmaf(1.061405429f, t, -1.453152027f);
   poly = fmaf(poly, t, 1.421413741f);
   poly = fmaf(poly, t, -0.284496736f);
   poly = fmaf(poly, t, 0.254829592f);
-  poly *= t;
-  const float q = poly * __expf(-z * z);
-  const float half_uq = 0.5f * u * q;
-  return u >= 0.f ? u - half_uq : half_uq;
+  const float w = (-0.5f * fabsf(u)) * t * e;
+  return fmaf(w, poly, fmaxf(u, 0.f));
 }
 // silu(u) = u / (1 + exp(-u)); for large negative u the denominator
 // overflows to +inf and the quotient is 0.
@@ -407,9 +414,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else bulk_wait_read<OUT_BUFS - 1>();
           }
           __syncwarp();
+          // 64-byte swizzle (the layout of the store's tensor map): 16-byte
+          // chunk q of row r sits at chunk q ^ ((r >> 1) & 3), so the 32
+          // rows' writes of one chunk hit all 32 banks (4 wavefronts, not 16)
           uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
+          const int sw = (lane >> 1) & 3;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = pk[q];
+          for (int q = 0; q < 4; ++q) dst[q ^ sw] = pk[q];
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -491,7 +502,7 @@ bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows) {
   cuuint32_t box[2] = {32, 32};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
