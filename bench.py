@@ -78,7 +78,8 @@ def load_peaks():
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "timestamp")
 
     def __init__(self, index):
         self.index = index
@@ -89,7 +90,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -107,18 +108,26 @@ class ClockSampler:
         rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                stamp, frac = parts[9].rsplit(".", 1)
+                t = time.mktime(time.strptime(stamp, "%Y/%m/%d %H:%M:%S")) + float("0." + frac)
+                rows.append(dict(t=t, sm=float(parts[1]), smax=float(parts[2]), w=float(parts[3]),
+                                 mask=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
             except ValueError:
                 continue
         if not rows:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"])
-        # samples are ~100 ms apart; keep those after the warm-up began
+        # samples (~20 ms apart) taken while the timed steps ran
+        inside = [r for r in rows if self.t_start is not None and self.t_end is not None
+                  and self.t_start <= r["t"] <= self.t_end]
+        window = "timed region"
+        if len(inside) < 3:
+            inside, window = rows, "whole sampling period (timed region too short)"
         reasons = set()
-        for r in rows:
+        for r in inside:
             if r["hw"] == "Active":
                 reasons.add("hw_slowdown")
             if r["hwt"] == "Active":
@@ -127,10 +136,11 @@ class ClockSampler:
                 reasons.add("sw_thermal_slowdown")
             if r["pcap"] == "Active":
                 reasons.add("sw_power_cap")
-        loaded = [r["sm"] for r in rows if r["sm"] > 0]
-        return dict(sm_mhz=statistics.median(loaded) if loaded else None,
+        return dict(sm_mhz=statistics.median(r["sm"] for r in inside),
                     sm_max_mhz=max(r["smax"] for r in rows), reasons=sorted(reasons),
-                    samples=len(rows))
+                    power_w=statistics.median(r["w"] for r in inside),
+                    active_masks=sorted({r["mask"] for r in inside}),
+                    samples=len(inside), window=window)
 
 
 # ---------------------------------------------------------------- work model
@@ -319,11 +329,15 @@ def main():
         pg.barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.mark("start")
     ev0.record(stream)
     for i in range(args.steps):
         step(i)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.mark("end")
     if pg:
         pg.barrier()
     ms = ev0.elapsed_time(ev1) / args.steps

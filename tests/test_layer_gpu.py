@@ -24,6 +24,10 @@ SMALL = {
     "decode_small": W.small(WL["decode"], T=64, d=512, H=256),
     "drops_heavy": W.small(WL["longtail"], T=999, d=64, H=64, c=Fraction(1, 3)),
     "single_expert": W.small(WL["switch_top1"], T=77, d=64, H=128, E=1, k=1),
+    # >= 512 rows per expert on average: the grouped GEMM runs as CTA pairs
+    "switch_pairs": W.small(WL["switch_top1"], T=4100, d=256, H=512, E=4),
+    "mixtral_pairs": W.small(WL["mixtral"], T=2100, d=256, H=384, E=4),
+    "longtail_pairs": W.small(WL["longtail"], T=6000, d=128, H=192, E=16),
 }
 
 

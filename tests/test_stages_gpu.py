@@ -110,7 +110,7 @@ def test_dispatch_all_tokens_one_expert():
 
 def _ffn_case(E, d, H, act, dt, kept, seed):
     w = W.Workload("ffn", T=int(sum(kept)), d=d, E=E, k=1, H=H, act=act, dtype=dt,
-                   c=Fraction(E), expert_bias=(act == "gelu" and dt == "f32"), seed=seed)
+                   c=Fraction(E), expert_bias=(act == "gelu"), seed=seed)
     inp = W.make_inputs(w)
     if w.expert_bias:   # nonzero biases so that the bias path is exercised
         g = torch.Generator().manual_seed(seed + 7)
@@ -129,10 +129,17 @@ FFN_CASES = [
     (5, 136, 200, "swiglu", "bf16", [33, 0, 0, 140, 9]),    # ragged d, H
     (2, 2048, 1408, "swiglu", "bf16", [300, 45]),
     (1, 64, 64, "gelu", "bf16", [1]),
-    # 148 to 266 output tiles: the last wave is under 90 % full, so the
-    # grouped GEMM runs stream-K (tiles split between neighbouring CTAs)
+    # 148 to 266 output tiles: a second wave under 90 % full
     (2, 2048, 1024, "gelu", "bf16", [2400, 2300]),
     (2, 512, 1024, "swiglu", "bf16", [1300, 1290]),
+    # at least 512 rows per expert on average: CTA pairs with 256-row tiles;
+    # experts ending inside the first or the second CTA's half, a one-row
+    # expert (the second CTA has no valid row), an empty expert, ragged d, H
+    (2, 256, 512, "gelu", "bf16", [700, 333]),
+    (4, 512, 768, "swiglu", "bf16", [1, 1500, 0, 600]),
+    (3, 136, 200, "gelu", "bf16", [900, 700, 2]),
+    (3, 136, 200, "swiglu", "bf16", [900, 700, 2]),
+    (1, 1024, 1024, "gelu", "bf16", [3000]),
 ]
 
 
