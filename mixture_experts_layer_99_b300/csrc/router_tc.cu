@@ -103,14 +103,15 @@ __device__ __forceinline__ void router_tile_epilogue(
   for (int e = etid; e < EP; e += 128) es.hist[e] = 0;
   const int t = tile * BM + r;
   const bool valid = t < T;
-  // selection keys
+  // selection keys (one reciprocal of tau; tau = 1 leaves the logits as they are)
+  const float inv_tau = tau == 1.f ? 1.f : 1.f / tau;
 #pragma unroll
   for (int e = 0; e < EP; ++e) {
     float z = v[e];
     if (e < E && valid) {
       if (bias) z += __ldg(bias + e);
       if (noise) z += __ldg(noise + (size_t)t * E + e);
-      z = z / tau;
+      z *= inv_tau;
     }
     v[e] = e < E ? z : -INFINITY;
   }
@@ -175,13 +176,19 @@ __device__ __forceinline__ void router_tile_epilogue(
     }
   }
   // per-expert sums of p over the tile's tokens: butterfly in each warp,
-  // then the 4 warps in a fixed order
+  // then the 4 warps in a fixed order (all experts' butterflies interleaved)
+  const float inv_s = 1.f / s;
+  float pe[EP];
 #pragma unroll
-  for (int e = 0; e < EP; ++e) {
-    float pe = (valid && e < E) ? v[e] / s : 0.f;
+  for (int e = 0; e < EP; ++e) pe[e] = (valid && e < E) ? v[e] * inv_s : 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
-    if (lane == 0) es.red[quarter][e] = pe;
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e) pe[e] += __shfl_xor_sync(0xffffffffu, pe[e], o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e) es.red[quarter][e] = pe[e];
   }
   epi_bar();
   for (int e = etid; e < E; e += 128) {
