@@ -34,19 +34,24 @@ constexpr int BK = 64;
 constexpr int NUM_THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;
 
+// Epilogue scratch: the tile's probabilities, one padded row per token (an odd
+// row stride keeps both the row writes and the column reads conflict-free),
+// summed per expert down the columns.
+template <int EP>
+struct EpiSmem {
+  float col[BM][EP + 1];
+  float part[EP];
+  int hist[EP];
+};
+
 template <int EP>
 struct RouterCfg {
   static constexpr int B_BYTES = EP * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196 * 1024) / STAGE > 8 ? 8 : (196 * 1024) / STAGE;
+  // as many operand stages (at most 8) as fit beside the epilogue scratch
+  static constexpr int FIT = (int)((220 * 1024 - sizeof(EpiSmem<EP>) - 1024 - 256) / STAGE);
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr int TCOLS = 2 * EP <= 32 ? 32 : (2 * EP <= 64 ? 64 : 128);
-};
-
-template <int EP>
-struct EpiSmem {
-  float red[4][EP];
-  float part[EP];
-  int hist[EP];
 };
 
 template <int EP>
@@ -96,33 +101,63 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[EP]) {
 // tile's per-expert selection counts and sums of p (fixed order).
 template <int EP>
 __device__ __forceinline__ void router_tile_epilogue(
-    float (&v)[EP], int tile, int r, int lane, int quarter, int etid,
-    const float* __restrict__ bias, const float* __restrict__ noise, float tau, int T, int E,
-    int k, float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
-    int32_t* __restrict__ tile_hist, EpiSmem<EP>& es) {
+    float (&v)[EP], int tile, int r, int etid, const float* __restrict__ bias,
+    const float* __restrict__ noise, float tau, int T, int E, int k, float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ gate, int32_t* __restrict__ tile_hist,
+    EpiSmem<EP>& es) {
   for (int e = etid; e < EP; e += 128) es.hist[e] = 0;
   const int t = tile * BM + r;
   const bool valid = t < T;
-  // selection keys (one reciprocal of tau; tau = 1 leaves the logits as they are)
-  const float inv_tau = tau == 1.f ? 1.f : 1.f / tau;
+  const bool vec4 = (E & 3) == 0;  // rows of [T, E] fp32 arrays are 16-byte aligned
+  // selection keys l = (z + b + g) / tau (one reciprocal; tau = 1 leaves them as they are)
+  if (valid) {
+    if (bias) {
 #pragma unroll
-  for (int e = 0; e < EP; ++e) {
-    float z = v[e];
-    if (e < E && valid) {
-      if (bias) z += __ldg(bias + e);
-      if (noise) z += __ldg(noise + (size_t)t * E + e);
-      z *= inv_tau;
+      for (int e = 0; e < EP; ++e)
+        if (e < E) v[e] += __ldg(bias + e);
     }
-    v[e] = e < E ? z : -INFINITY;
+    if (noise) {
+      const float* nr = noise + (size_t)t * E;
+      if (vec4) {
+#pragma unroll
+        for (int e = 0; e < EP; e += 4) {
+          if (e < E) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(nr + e));
+            v[e] += q.x;
+            v[e + 1] += q.y;
+            v[e + 2] += q.z;
+            v[e + 3] += q.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+          if (e < E) v[e] += __ldg(nr + e);
+      }
+    }
+    if (tau != 1.f) {
+      const float inv_tau = 1.f / tau;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) v[e] *= inv_tau;
+    }
   }
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e >= E) v[e] = -INFINITY;
   float m = -INFINITY;
 #pragma unroll
   for (int e = 0; e < EP; ++e) m = fmaxf(m, v[e]);
   if (valid && logits) {
     float* lr = logits + (size_t)t * E;
+    if (vec4) {
 #pragma unroll
-    for (int e = 0; e < EP; ++e)
-      if (e < E) lr[e] = v[e];
+      for (int e = 0; e < EP; e += 4)
+        if (e < E) *reinterpret_cast<float4*>(lr + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e < E) lr[e] = v[e];
+    }
   }
   // top-k on the keys: descending, ties to the lower index
   uint64_t taken = 0;
@@ -149,20 +184,16 @@ __device__ __forceinline__ void router_tile_epilogue(
       seli[j] = bi;
     }
   }
-  float s = 0.f;
-#pragma unroll
-  for (int e = 0; e < EP; ++e) {
-    v[e] = e < E ? expf(v[e] - m) : 0.f;
-    s += v[e];
-  }
   __syncwarp();
-  epi_bar();  // hist zeroed
+  epi_bar();  // hist zeroed; the previous tile's column sums are done
   if (valid) {
+    // gates from the selected keys only: g_j = p_j / sum_m p_m, where the
+    // softmax denominator cancels
     float psel[kMaxK], psum = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       if (j < k) {
-        psel[j] = expf(selv[j] - m) / s;
+        psel[j] = expf(selv[j] - m);
         psum += psel[j];
       }
     }
@@ -175,24 +206,29 @@ __device__ __forceinline__ void router_tile_epilogue(
       }
     }
   }
-  // per-expert sums of p over the tile's tokens: butterfly in each warp,
-  // then the 4 warps in a fixed order (all experts' butterflies interleaved)
-  const float inv_s = 1.f / s;
-  float pe[EP];
+  // probabilities for the statistics P_i: one row per token in shared memory
+  {
+    float s = 0.f;
 #pragma unroll
-  for (int e = 0; e < EP; ++e) pe[e] = (valid && e < E) ? v[e] * inv_s : 0.f;
+    for (int e = 0; e < EP; ++e) {
+      v[e] = (e < E && valid) ? __expf(v[e] - m) : 0.f;
+      s += v[e];
+    }
+    const float inv_s = valid ? 1.f / s : 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-    for (int e = 0; e < EP; ++e) pe[e] += __shfl_xor_sync(0xffffffffu, pe[e], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int e = 0; e < EP; ++e) es.red[quarter][e] = pe[e];
+    for (int e = 0; e < EP; ++e) es.col[r][e] = v[e] * inv_s;
   }
   epi_bar();
+  // per-expert sums over the tile's 128 tokens: one thread per expert walks
+  // its column in token order (two interleaved partial sums, then added)
   for (int e = etid; e < E; e += 128) {
-    es.part[e] += ((es.red[0][e] + es.red[1][e]) + es.red[2][e]) + es.red[3][e];
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+    for (int rr = 0; rr < BM; rr += 2) {
+      a0 += es.col[rr][e];
+      a1 += es.col[rr + 1][e];
+    }
+    es.part[e] += a0 + a1;
     if (tile_hist) tile_hist[(size_t)tile * E + e] = es.hist[e];
   }
   epi_bar();
@@ -363,8 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (e < E) pr[e] = v[e];
         }
       } else {
-        router_tile_epilogue<EP>(v, tile, r, lane, quarter, etid, bias, noise, tau, T, E, k,
-                                 logits, idx, gate, tile_hist, st.epi);
+        router_tile_epilogue<EP>(v, tile, r, etid, bias, noise, tau, T, E, k, logits, idx, gate,
+                                 tile_hist, st.epi);
       }
     }
     if (!SPLIT)
@@ -388,7 +424,7 @@ __global__ void __launch_bounds__(128) router_split_epilogue(
     float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
     float* __restrict__ partial, int32_t* __restrict__ tile_hist) {
   __shared__ EpiSmem<EP> es;
-  const int tid = threadIdx.x, lane = tid & 31, quarter = tid >> 5;
+  const int tid = threadIdx.x;
   const int tile = blockIdx.x;
   for (int e = tid; e < EP; e += 128) es.part[e] = 0.f;
   pdl_wait();
@@ -418,8 +454,8 @@ __global__ void __launch_bounds__(128) router_split_epilogue(
     }
   }
   __syncthreads();
-  router_tile_epilogue<EP>(v, tile, tid, lane, quarter, tid, bias, noise, tau, T, E, k, logits,
-                           idx, gate, tile_hist, es);
+  router_tile_epilogue<EP>(v, tile, tid, tid, bias, noise, tau, T, E, k, logits, idx, gate,
+                           tile_hist, es);
   for (int e = tid; e < E; e += 128) partial[(size_t)tile * E + e] = es.part[e];
 }
 
