@@ -35,7 +35,9 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 
 // One block of 256 threads per 128-token tile.
 //  1. tot[e] = slots of e in all tiles, base[e] = slots of e in earlier tiles
-//     (a coalesced pass over the router's [tiles, E] counts, integer atomics);
+//     (thread j sums expert j % E over every G-th tile, G = 256 / E, with
+//     coalesced reads of the router's [tiles, E] counts; then the G partials
+//     of each expert are added);
 //  2. offset_e = sum_{e'<e} min(tot_e', C);
 //  3. block 0 writes counts, offsets and the statistics;
 //  4. stable positions: warp w owns tokens [16w, 16w + 16) of the tile (16k
@@ -56,21 +58,37 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
   __shared__ double psum[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int tile = blockIdx.x;
-  for (int e = tid; e < kMaxE; e += 256) {
-    tot[e] = 0;
-    base[e] = 0;
-  }
   for (int i = tid; i < 8 * kMaxE; i += 256) (&wcnt[0][0])[i] = 0;
   pdl_wait();
-  __syncthreads();
-  const int nh = ntiles * E;
-  for (int i = tid; i < nh; i += 256) {
-    const int v = tile_hist[i];
-    if (v) {
-      const int tt = i / E, e = i - tt * E;
-      atomicAdd(&tot[e], v);
-      if (tt < tile) atomicAdd(&base[e], v);
+  {
+    // partial sums per (group g, expert e) into wcnt (as [2][G][E] ints),
+    // then tot/base per expert; integer sums, so the order is immaterial
+    const int G = 256 / E;  // E <= 256
+    int* ptot = &wcnt[0][0];
+    int* pbase = ptot + 256;
+    if (tid < G * E) {
+      const int e = tid % E, g = tid / E;
+      int st = 0, sb = 0;
+      for (int tt = g; tt < ntiles; tt += G) {
+        const int v = tile_hist[(size_t)tt * E + e];
+        st += v;
+        if (tt < tile) sb += v;
+      }
+      ptot[g * E + e] = st;
+      pbase[g * E + e] = sb;
     }
+    __syncthreads();
+    if (tid < E) {
+      int st = 0, sb = 0;
+      for (int g = 0; g < G; ++g) {
+        st += ptot[g * E + tid];
+        sb += pbase[g * E + tid];
+      }
+      tot[tid] = st;
+      base[tid] = sb;
+    }
+    __syncthreads();
+    for (int i = tid; i < 2 * 256; i += 256) (&wcnt[0][0])[i] = 0;
   }
   __syncthreads();
   if (w == 0) {
