@@ -164,13 +164,15 @@ def footprint_bytes(inp):
     return sum(v.numel() * v.element_size() for v in inp.values() if v is not None)
 
 
-def traffic_record(kernel_src_sha):
+def traffic_record(kernel_src_sha, workload):
+    """The committed ncu DRAM traffic of the grouped GEMM, if it was taken on
+    this workload from the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    if rec.get("source_sha256") != kernel_src_sha:
+    if rec.get("source_sha256") != kernel_src_sha or rec.get("workload") != workload:
         return None
     return rec
 
@@ -409,7 +411,7 @@ def main():
     gemm_ms = st["gemm1"] + st["gemm2"]
     achieved = work["gemm_flops"] / (gemm_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
-    rec = traffic_record(source_sha())
+    rec = traffic_record(source_sha(), w.name)
     g1_flops = work["gemm_flops"] * (w.nmat - 1) / w.nmat
     g2_flops = work["gemm_flops"] / w.nmat
     roof = dict(kernel="grouped_gemm_tc_kernel (GEMM1 + GEMM2 launches per layer call)",

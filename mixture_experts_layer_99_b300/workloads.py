@@ -19,9 +19,16 @@ The five workloads follow the shapes the MoE pages use:
   -log(-log(u)) supplied as an input tensor (lpnh.cn guide, sections 2.2/3.3).
 * ``decode``      - decode-like step, T=64, d=4096, E=64, k=2, SwiGLU
   4096->1408->4096, no drops.
+* ``sweep_e16_k4`` - the 16-expert, top-4 point of the expert-count x
+  active-count sweep of the intelliparadigm tutorial (section 2.1), with the
+  switch layer's total hidden width split over 16 experts (GELU
+  1024->2048->1024), c=1.25, and Gaussian router noise of standard deviation
+  0.05 added to the logits (the ``noise_std`` of the kwkr.cn MoE article,
+  section 3.3, whose typical range is 0.01 to 0.1).
 
 Draw order (one ``torch.Generator('cpu')`` per workload, seeded): x, W_g, W1,
-W3 (SwiGLU only), W2, then u for the Gumbel noise. All normal draws are fp32
+W3 (SwiGLU only), W2, then the router noise (u for Gumbel noise, or a
+standard normal draw scaled by ``noise_std``). All normal draws are fp32
 ``randn``; weights are scaled by 1/sqrt(fan_in) and then cast to the workload
 dtype. Weights use the ``nn.Linear`` storage convention [out, in]:
 W_g [E, d], W1 and W3 [E, H, d], W2 [E, d, H].
@@ -49,7 +56,8 @@ class Workload:
     c: Fraction              # capacity factor, exact
     expert_bias: bool = False    # b1 [E,H], b2 [E,d] present (zeros)
     router_bias: Optional[str] = None   # None or "zipf"
-    noise: Optional[str] = None         # None or "gumbel"
+    noise: Optional[str] = None         # None, "gumbel" or "gaussian"
+    noise_std: float = 0.0              # standard deviation of "gaussian" noise
     tau: float = 1.0
     seed: int = 0
     shared_H: int = 0                   # > 0: a shared expert of this hidden size
@@ -82,6 +90,9 @@ WORKLOADS = {
                          router_bias="zipf", noise="gumbel", tau=1.0),
     "decode": Workload("decode", T=64, d=4096, E=64, k=2, H=1408,
                        act="swiglu", dtype="bf16", c=Fraction(32)),
+    "sweep_e16_k4": Workload("sweep_e16_k4", T=8192, d=1024, E=16, k=4, H=2048,
+                             act="gelu", dtype="bf16", c=Fraction(5, 4),
+                             noise="gaussian", noise_std=0.05),
     # the long-tail layer plus one always-on shared expert of the same width
     "longtail_shared": Workload("longtail_shared", T=32768, d=2048, E=64, k=2, H=1408,
                                 act="swiglu", dtype="bf16", c=Fraction(2),
@@ -132,6 +143,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
         u = torch.rand(w.T, w.E, generator=gen, dtype=torch.float64)
         u = u.clamp_(1e-12, 1.0 - 1e-12)
         noise = (-torch.log(-torch.log(u))).to(torch.float32)
+    elif w.noise == "gaussian":
+        noise = _randn(gen, (w.T, w.E), w.noise_std, torch.float32)
     out = dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, b1=b1, b2=b2, bias=bias, noise=noise)
     if w.shared_H > 0:   # drawn last, so the routed inputs do not change
         Hs = w.shared_H

@@ -28,6 +28,9 @@ SMALL = {
     "switch_pairs": W.small(WL["switch_top1"], T=4100, d=256, H=512, E=4),
     "mixtral_pairs": W.small(WL["mixtral"], T=2100, d=256, H=384, E=4),
     "longtail_pairs": W.small(WL["longtail"], T=6000, d=128, H=192, E=16),
+    # 16 experts, top-4, Gaussian router noise
+    "sweep_small": W.small(WL["sweep_e16_k4"], T=2048, d=256, H=512),
+    "sweep_small_single_cta": W.small(WL["sweep_e16_k4"], T=1000, d=128, H=256),
 }
 
 
@@ -43,7 +46,7 @@ def test_layer_seeds(seed):
 
 
 FULL = {"ref_fp32": None, "switch_top1": 2048, "decode": None, "longtail": 1024,
-        "mixtral": 128}
+        "mixtral": 128, "sweep_e16_k4": 1024}
 
 
 @pytest.mark.parametrize("name", list(FULL))
