@@ -272,6 +272,47 @@ MOE_API moe_status_t moe_layer_forward_profiled(const moe_config_t *cfg,
                                                 size_t ws_bytes, moe_stream_t stream,
                                                 void *const *stage_events);
 
+/* ------------------------------------------------------------------ backward
+ * Gradients of loss = sum_t <dy_t, y_t> + alpha * L_balance through the layer
+ * computed by moe_layer_forward (the pages train the layer with the balance
+ * statistic added to the task loss: the kwkr.cn MoE article, section 2.2;
+ * the router is trained with it, section 3.3). The chain rule runs through
+ * the combine, the renormalised gates, the balance term (f is piecewise
+ * constant, P_i carries the gradient), the softmax, the router GEMM, the
+ * experts and the dispatch; selection, capacity and drops get no gradient.
+ * Weight gradients are fp32; dx has the layer dtype. */
+typedef struct {
+  void *dx;       /* [T, d] layer dtype, required                          */
+  float *dWg;     /* [E, d] required                                       */
+  float *dbias;   /* [E]    required iff in->bias, else NULL               */
+  float *dW1;     /* [E, H, d] required                                    */
+  float *dW3;     /* [E, H, d] SwiGLU (required), else NULL                */
+  float *dW2;     /* [E, d, H] required                                    */
+  float *db1;     /* [E, H] GELU: required iff in->b1, else NULL           */
+  float *db2;     /* [E, d] GELU: required iff in->b2, else NULL           */
+} moe_layer_grads_t;
+
+/* Bytes of the backward workspace (its own buffer, 256-byte aligned; zero its
+ * header once with moe_workspace_init; moe_device_status reads it). Host only.
+ * MOE_ERR_UNSUPPORTED for shapes the backward does not cover. */
+MOE_API moe_status_t moe_workspace_size_backward(const moe_config_t *cfg, size_t *bytes);
+
+/* Backward of one moe_layer_forward call. Enqueue it on the forward's stream
+ * after the forward, with the same cfg, in, ws and outputs `fwd`, before
+ * anything else reuses ws: it reads the forward's routing (fwd->logits,
+ * topk_idx, topk_gate, slot_of, expert_offset and f must all be non-NULL),
+ * the gathered rows and, for k > 1, the expert outputs kept in ws. dy [T, d]
+ * is the upstream gradient of y (layer dtype); alpha the weight of
+ * L_balance. The expert pre-activations are recomputed. Every sum is taken in
+ * a fixed order (results are run-to-run identical). Covered: bf16 with
+ * E <= 64 (the tensor-core forward); no shared expert. Nothing is enqueued
+ * on a validation failure. */
+MOE_API moe_status_t moe_layer_backward(const moe_config_t *cfg, const moe_layer_inputs_t *in,
+                                        const moe_layer_outputs_t *fwd, const void *dy,
+                                        float alpha, const moe_layer_grads_t *grads,
+                                        const void *ws, size_t ws_bytes, void *bwd_ws,
+                                        size_t bwd_ws_bytes, moe_stream_t stream);
+
 /* Number of kernels one moe_layer_forward call launches for this shape
  * (0 if cfg is invalid). Host only. */
 MOE_API int32_t moe_layer_forward_launch_count(const moe_config_t *cfg);

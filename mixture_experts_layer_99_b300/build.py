@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_tiles.cu", "dispatch_static.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu"]
+SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_tiles.cu", "dispatch_static.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu", "backward.cu", "ffn_wgrad_tc.cu"]
 
 
 def nvcc_path() -> str:

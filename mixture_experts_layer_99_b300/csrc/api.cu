@@ -461,4 +461,132 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- backward
+namespace {
+struct BwdLayout {
+  size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W2T, W13T, dz, dg, wg_part,
+      wg_bpart, total;
+  int64_t rp;  // padded packed-row bound (columns of the transposed operands)
+};
+BwdLayout bwd_layout(const moe_config_t& c) {
+  BwdLayout L;
+  memset(&L, 0, sizeof(L));
+  const size_t R = (size_t)max_rows(c), E = (size_t)c.E, d = (size_t)c.d, H = (size_t)c.H;
+  const size_t Hp = c.act == MOE_ACT_SWIGLU ? 2 * H : H;
+  L.rp = (int64_t)align_up(R + 64 * E, 64);
+  const size_t rp = (size_t)L.rp;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return at;
+  };
+  L.hdr = take(kHdrBytes);
+  L.pre = take(R * Hp * 2);
+  L.dact = take(R * Hp * 2);
+  L.dY = take(R * d * 2);
+  L.dxd = take(R * d * 2);
+  L.poff = take((E + 1) * 4);
+  L.tdY = take(d * rp * 2);
+  L.th = take(H * rp * 2);
+  L.tdact = take(Hp * rp * 2);
+  L.txd = take(d * rp * 2);
+  L.W2T = take(E * H * d * 2);
+  L.W13T = take(E * d * Hp * 2);
+  L.dz = take((size_t)c.T * E * 4);
+  L.dg = take((size_t)c.T * (size_t)c.k * 4);
+  L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
+  L.wg_bpart = take((size_t)bwd_wg_splits(c) * E * 4);
+  L.total = off;
+  return L;
+}
+bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && router_tc_supported(c); }
+}  // namespace
+
+moe_status_t moe_workspace_size_backward(const moe_config_t* cfg, size_t* bytes) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (!bwd_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  *bytes = bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                const moe_layer_outputs_t* fwd, const void* dy, float alpha,
+                                const moe_layer_grads_t* g, const void* ws, size_t ws_bytes,
+                                void* bws, size_t bws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config_t& c = *cfg;
+  if (!bwd_supported(c)) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if (!in->x || !fwd || !dy || !g) return MOE_ERR_INVALID_ARG;
+  if (!fwd->logits || !fwd->topk_idx || !fwd->topk_gate || !fwd->slot_of ||
+      !fwd->expert_offset || !fwd->f)
+    return MOE_ERR_INVALID_ARG;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (!g->dx || !g->dWg || !g->dW1 || !g->dW2 || (swiglu != (g->dW3 != nullptr)) ||
+      ((in->bias != nullptr) != (g->dbias != nullptr)) ||
+      ((in->b1 != nullptr) != (g->db1 != nullptr)) ||
+      ((in->b2 != nullptr) != (g->db2 != nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c, 0);
+  if ((st = check_ws(const_cast<void*>(ws), ws_bytes, L.total_layer)) != MOE_OK) return st;
+  const BwdLayout B = bwd_layout(c);
+  if ((st = check_ws(bws, bws_bytes, B.total)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t R = max_rows(c);
+  const int Hp = swiglu ? 2 * c.H : c.H;
+  int32_t* hdr = at<int32_t>(bws, 0);
+  void* wsm = const_cast<void*>(ws);
+  const void* xd = at<void>(wsm, L.xd);
+  const void* Y = c.k > 1 ? at<void>(wsm, L.Y) : nullptr;  // k = 1: gates are identically 1
+  const int32_t* off = fwd->expert_offset;
+  void* pre = at<void>(bws, B.pre);
+  void* dact = at<void>(bws, B.dact);
+  void* dYb = at<void>(bws, B.dY);
+  void* dxd = at<void>(bws, B.dxd);
+  int32_t* poff = at<int32_t>(bws, B.poff);
+  void* W2T = at<void>(bws, B.W2T);
+  void* W13T = at<void>(bws, B.W13T);
+  float* dz = at<float>(bws, B.dz);
+  float* dg = at<float>(bws, B.dg);
+  const int ldp = (int)B.rp;
+  cudaError_t e = launch_weight_transpose(in->W2, c.E, c.d, c.H, c.d, 0, W2T, s);
+  if (e == cudaSuccess) e = launch_weight_transpose(in->W1, c.E, c.H, c.d, Hp, 0, W13T, s);
+  if (e == cudaSuccess && swiglu)
+    e = launch_weight_transpose(in->W3, c.E, c.H, c.d, Hp, c.H, W13T, s);
+  if (e == cudaSuccess) e = launch_bwd_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s);
+  if (e == cudaSuccess)
+    e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz, s);
+  if (e == cudaSuccess)
+    e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, W2T, W13T, dYb, pre, dact, dxd, R,
+                          hdr, s);
+  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dz, in->Wg, g->dx, s);
+  if (e == cudaSuccess)
+    e = launch_bwd_wg(c, dz, in->x, at<float>(bws, B.wg_part), at<float>(bws, B.wg_bpart), g->dWg,
+                      g->dbias, s);
+  if (e == cudaSuccess) e = launch_pad_offsets(off, c.E, poff, s);
+  if (e == cudaSuccess)
+    e = launch_transpose_pad(0, dYb, c.d, c.d, off, poff, c.E, B.rp, at<void>(bws, B.tdY), ldp, s);
+  if (e == cudaSuccess)
+    e = launch_transpose_pad(swiglu ? 2 : 1, pre, Hp, c.H, off, poff, c.E, B.rp,
+                             at<void>(bws, B.th), ldp, s);
+  if (e == cudaSuccess)
+    e = launch_transpose_pad(0, dact, Hp, Hp, off, poff, c.E, B.rp, at<void>(bws, B.tdact), ldp, s);
+  if (e == cudaSuccess)
+    e = launch_transpose_pad(0, xd, c.d, c.d, off, poff, c.E, B.rp, at<void>(bws, B.txd), ldp, s);
+  // dW2 [E, d, H] = dY^T h;  [dW1; dW3] [E, Hp, d] = dact^T xd
+  if (e == cudaSuccess)
+    e = launch_wgrad_tc(at<void>(bws, B.tdY), at<void>(bws, B.th), B.rp, poff, c.E, c.d, c.H, c.d,
+                        g->dW2, g->dW2, hdr, s);
+  if (e == cudaSuccess)
+    e = launch_wgrad_tc(at<void>(bws, B.tdact), at<void>(bws, B.txd), B.rp, poff, c.E, Hp, c.d,
+                        c.H, g->dW1, swiglu ? g->dW3 : g->dW1, hdr, s);
+  if (e == cudaSuccess && g->db1) e = launch_expert_colsum(dact, Hp, c.H, off, c.E, g->db1, s);
+  if (e == cudaSuccess && g->db2) e = launch_expert_colsum(dYb, c.d, c.d, off, c.E, g->db2, s);
+  return cuda_status(e);
+}
+
 }  // extern "C"

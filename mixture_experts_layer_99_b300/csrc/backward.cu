@@ -1,0 +1,433 @@
+// Backward pass of the layer: the memory-bound steps (CUDA cores).
+//
+// loss = sum_t <dy_t, y_t> + alpha * L_balance. The kwkr.cn MoE article ("MoE
+// sparse activation: from the math to the code") trains the layer with
+// L_balance added to the task loss (section 2.2) and trains the router
+// (section 3.3); the gradients are the chain rule through its forward:
+//   combine      dY[slot] = g_tj dy_t,  dg_tj = <dy_t, Y[slot]>
+//   gates        dp_{K_i} += (dg_i - sum_j g_j dg_j) / S,  S = sum_m p_{K_m}
+//   balance      dp_ti += alpha E f_i / T
+//   softmax      dl_t = p_t (dp_t - <p_t, dp_t>),  dz = dl / tau
+//   router GEMM  dx += dz Wg,  dWg = dz^T x,  db = sum_t dz_t
+//   dispatch     dx_t += sum over the kept slots of t of dxd[slot]
+// Routing (top-k, capacity, drops) is piecewise constant and gets no gradient.
+// Every sum runs in a fixed order, so results are run-to-run identical.
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int NT = 256, NW = NT / 32;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+// One warp per token: dY rows of its kept slots and the gate gradients.
+// Y (the forward's expert outputs) may be null when k = 1: a single gate is
+// identically 1 and its gradient has no effect.
+__global__ void __launch_bounds__(NT) bwd_combine_kernel(const uint4* __restrict__ dy,
+                                                         const uint4* __restrict__ Y,
+                                                         const int32_t* __restrict__ slot_of,
+                                                         const float* __restrict__ gate, int T,
+                                                         int k, int nvec,
+                                                         uint4* __restrict__ dY,
+                                                         float* __restrict__ dg) {
+  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  for (int j = 0; j < k; ++j) {
+    const int sl = slot_of[(size_t)t * k + j];
+    const float g = gate[(size_t)t * k + j];
+    float dot = 0.f;
+    if (sl >= 0) {
+      for (int v = lane; v < nvec; v += 32) {
+        float a[8], o[8];
+        unpack8(__ldg(dy + (size_t)t * nvec + v), a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = g * a[i];
+        dY[(size_t)sl * nvec + v] = pack8(o);
+        if (Y) {
+          float b[8];
+          unpack8(__ldg(Y + (size_t)sl * nvec + v), b);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dot = fmaf(a[i], b[i], dot);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) dg[(size_t)t * k + j] = dot;
+  }
+}
+
+// One thread per token: dz[t, :] from the gates' gradients and the balance
+// term, through the softmax of the saved keys (logits).
+template <int EP>
+__global__ void __launch_bounds__(128) bwd_router_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ gate, const float* __restrict__ dg,
+    const float* __restrict__ f, float alpha, float tau, int T, int E, int k,
+    float* __restrict__ dz) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  float p[EP];
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    p[e] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    m = fmaxf(m, p[e]);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    p[e] = e < E ? expf(p[e] - m) : 0.f;
+    s += p[e];
+  }
+  const float inv_s = 1.f / s;
+  // dp = balance term + gate term on the chosen experts
+  float dp[EP];
+  const float bal = alpha * (float)E / (float)T;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    p[e] *= inv_s;
+    dp[e] = e < E ? bal * f[e] : 0.f;
+  }
+  float S = 0.f, gdg = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(size_t)t * k + j];
+    float pe = 0.f;
+#pragma unroll
+    for (int q = 0; q < EP; ++q)
+      if (q == e) pe = p[q];
+    S += pe;
+    gdg = fmaf(gate[(size_t)t * k + j], dg[(size_t)t * k + j], gdg);
+  }
+  const float inv_S = 1.f / S;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(size_t)t * k + j];
+    const float add = (dg[(size_t)t * k + j] - gdg) * inv_S;
+#pragma unroll
+    for (int q = 0; q < EP; ++q)
+      if (q == e) dp[q] += add;
+  }
+  float pdp = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) pdp = fmaf(p[e], dp[e], pdp);
+  const float inv_tau = 1.f / tau;
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e < E) dz[(size_t)t * E + e] = p[e] * (dp[e] - pdp) * inv_tau;
+}
+
+// One warp per token: dx_t = sum over kept slots of dxd[slot] (slot order)
+// + sum_e dz[t, e] Wg[e, :] (expert order), fp32, rounded once.
+__global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dxd,
+                                                    const int32_t* __restrict__ slot_of,
+                                                    const float* __restrict__ dz,
+                                                    const uint4* __restrict__ Wg, int T, int k,
+                                                    int E, int nvec, uint4* __restrict__ dx) {
+  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const int sl = slot_of[(size_t)t * k + j];
+      if (sl < 0) continue;
+      float a[8];
+      unpack8(__ldg(dxd + (size_t)sl * nvec + v), a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += a[i];
+    }
+    for (int e = 0; e < E; ++e) {
+      const float z = __ldg(dz + (size_t)t * E + e);
+      float w[8];
+      unpack8(__ldg(Wg + (size_t)e * nvec + v), w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(z, w[i], acc[i]);
+    }
+    dx[(size_t)t * nvec + v] = pack8(acc);
+  }
+}
+
+// dWg = dz^T x and db = sum_t dz: block (column block cb, token split sp)
+// writes the partial sums of its tokens; thread c owns column cb*128 + c and
+// all E experts. dz of 32 tokens is staged in shared memory at a time.
+constexpr int WG_COLS = 128, WG_TOK = 32;
+template <int EP>
+__global__ void __launch_bounds__(WG_COLS) bwd_wg_partial_kernel(
+    const float* __restrict__ dz, const __nv_bfloat16* __restrict__ x, int T, int d, int E,
+    int tok_per_split, float* __restrict__ part, float* __restrict__ bpart) {
+  __shared__ float sdz[WG_TOK][EP];
+  const int c = blockIdx.x * WG_COLS + threadIdx.x;
+  const int sp = blockIdx.y;
+  const int t0 = sp * tok_per_split;
+  const int t1 = min(T, t0 + tok_per_split);
+  float acc[EP];
+  float bacc = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+  for (int tb = t0; tb < t1; tb += WG_TOK) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < WG_TOK * EP; i += WG_COLS) {
+      const int tt = tb + i / EP, e = i % EP;
+      sdz[i / EP][e] = (tt < t1 && e < E) ? dz[(size_t)tt * E + e] : 0.f;
+    }
+    __syncthreads();
+    const int n = min(WG_TOK, t1 - tb);
+    for (int i = 0; i < n; ++i) {
+      const float xv = c < d ? __bfloat162float(x[(size_t)(tb + i) * d + c]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[e] = fmaf(sdz[i][e], xv, acc[e]);
+      if (threadIdx.x < EP) bacc += sdz[i][threadIdx.x];
+    }
+  }
+  if (c < d) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E) part[((size_t)sp * E + e) * d + c] = acc[e];
+  }
+  if (blockIdx.x == 0 && threadIdx.x < E) bpart[(size_t)sp * E + threadIdx.x] = bacc;
+}
+
+// Sum of the token-split partials in split order.
+__global__ void bwd_wg_reduce_kernel(const float* __restrict__ part,
+                                     const float* __restrict__ bpart, int nsplit, int E, int d,
+                                     float* __restrict__ dWg, float* __restrict__ dbias) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = E * d;
+  if (i < n) {
+    float s = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) s += part[(size_t)sp * n + i];
+    dWg[i] = s;
+  }
+  if (dbias && i < E) {
+    float s = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) s += bpart[(size_t)sp * E + i];
+    dbias[i] = s;
+  }
+}
+
+// Padded expert offsets: poff_0 = 0, poff_{e+1} = poff_e + roundup(rows_e, 64).
+__global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int E,
+                                   int32_t* __restrict__ poff) {
+  if (threadIdx.x != 0) return;
+  int run = 0;
+  poff[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    const int n = off[e + 1] - off[e];
+    run += (n + 63) / 64 * 64;
+    poff[e + 1] = run;
+  }
+}
+
+// out[c, p] = act(in rows) transposed into the padded expert layout: packed
+// row r of expert e (r in [off_e, off_{e+1})) goes to column
+// poff_e + (r - off_e); the columns up to the next multiple of 64 are zero.
+// ACT 0: copy of in[:, c]; 1: gelu(in[:, c]); 2: silu(in[:, c]) * in[:, C + c]
+// (the SwiGLU hidden row from the packed [gate | up] pre-activations).
+// Block = 64 padded columns x 64 channels; a 64-column block never straddles
+// two experts because every poff_e is a multiple of 64.
+template <int ACT>
+__global__ void __launch_bounds__(256) transpose_pad_kernel(
+    const __nv_bfloat16* __restrict__ in, int ld_in, int C, const int32_t* __restrict__ off,
+    const int32_t* __restrict__ poff, int E, __nv_bfloat16* __restrict__ out, int ld_out) {
+  __shared__ float tile[64][65];
+  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  if (p0 >= poff[E]) return;
+  int lo = 0, hi = E - 1;  // expert with poff_e <= p0 < poff_{e+1}
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (poff[mid] <= p0) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo;
+  const int local = p0 - poff[e];
+  const int nvalid = min(64, off[e + 1] - off[e] - local);
+  const int r0 = off[e] + local;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+  for (int i = ty; i < 64; i += 4) {
+    float v = 0.f;
+    const int c = c0 + tx;
+    if (i < nvalid && c < C) {
+      const __nv_bfloat16* rp = in + (size_t)(r0 + i) * ld_in;
+      const float a = __bfloat162float(rp[c]);
+      if (ACT == 0) {
+        v = a;
+      } else if (ACT == 1) {
+        v = 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+      } else {
+        const float u = __bfloat162float(rp[C + c]);
+        v = a / (1.f + expf(-a)) * u;
+      }
+    }
+    tile[i][tx] = v;
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 4) {
+    const int c = c0 + i;
+    if (c < C) out[(size_t)c * ld_out + p0 + tx] = __float2bfloat16_rn(tile[tx][i]);
+  }
+}
+
+// Batched transpose of expert weights: out[e][b][a + a_off] = in[e][a][b]
+// (in [E, A, B] row-major, out [E, B, ld_out]).
+__global__ void __launch_bounds__(256) weight_transpose_kernel(
+    const __nv_bfloat16* __restrict__ in, int A, int B, int ld_out, int a_off,
+    __nv_bfloat16* __restrict__ out) {
+  __shared__ __nv_bfloat16 tile[64][66];
+  const int e = blockIdx.z;
+  const int a0 = blockIdx.y * 64, b0 = blockIdx.x * 64;
+  const __nv_bfloat16* ie = in + (size_t)e * A * B;
+  __nv_bfloat16* oe = out + (size_t)e * B * ld_out;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  for (int i = ty; i < 64; i += 4) {
+    const int a = a0 + i, b = b0 + tx;
+    tile[i][tx] = (a < A && b < B) ? ie[(size_t)a * B + b] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 4) {
+    const int b = b0 + i, a = a0 + tx;
+    if (a < A && b < B) oe[(size_t)b * ld_out + a_off + a] = tile[tx][i];
+  }
+}
+
+// Per-expert column sums of a packed [rows, C] matrix (row stride ld) over the
+// expert's rows, in row order: out[e, c] (fp32).
+__global__ void __launch_bounds__(128) expert_colsum_kernel(const __nv_bfloat16* __restrict__ a,
+                                                            int ld, int C,
+                                                            const int32_t* __restrict__ off,
+                                                            float* __restrict__ out) {
+  const int e = blockIdx.y;
+  const int c = blockIdx.x * 128 + threadIdx.x;
+  if (c >= C) return;
+  float s = 0.f;
+  for (int r = off[e]; r < off[e + 1]; ++r) s += __bfloat162float(a[(size_t)r * ld + c]);
+  out[(size_t)e * C + c] = s;
+}
+
+template <int EP>
+cudaError_t launch_router_bwd_ep(const moe_config_t& c, const float* logits, const int32_t* idx,
+                                 const float* gate, const float* dg, const float* f, float alpha,
+                                 float* dz, cudaStream_t s) {
+  bwd_router_kernel<EP><<<(c.T + 127) / 128, 128, 0, s>>>(logits, idx, gate, dg, f, alpha, c.tau,
+                                                          c.T, c.E, c.k, dz);
+  return cudaGetLastError();
+}
+
+template <int EP>
+cudaError_t launch_wg_ep(const moe_config_t& c, const float* dz, const void* x, int nsplit,
+                         int tok_per_split, float* part, float* bpart, cudaStream_t s) {
+  const dim3 grid((unsigned)((c.d + WG_COLS - 1) / WG_COLS), (unsigned)nsplit);
+  bwd_wg_partial_kernel<EP><<<grid, WG_COLS, 0, s>>>(
+      dz, static_cast<const __nv_bfloat16*>(x), c.T, c.d, c.E, tok_per_split, part, bpart);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int bwd_wg_splits(const moe_config_t& c) {
+  const int per = 256;  // tokens per split
+  int n = (c.T + per - 1) / per;
+  return n < 1 ? 1 : n;
+}
+
+cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
+                               const int32_t* slot_of, const float* gate, void* dY, float* dg,
+                               cudaStream_t s) {
+  const int nvec = c.d / 8;
+  bwd_combine_kernel<<<(c.T + NW - 1) / NW, NT, 0, s>>>(
+      static_cast<const uint4*>(dy), static_cast<const uint4*>(Y), slot_of, gate, c.T, c.k, nvec,
+      static_cast<uint4*>(dY), dg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
+                              const float* gate, const float* dg, const float* f, float alpha,
+                              float* dz, cudaStream_t s) {
+  const int ep = (c.E + 15) / 16 * 16;
+  switch (ep) {
+    case 16: return launch_router_bwd_ep<16>(c, logits, idx, gate, dg, f, alpha, dz, s);
+    case 32: return launch_router_bwd_ep<32>(c, logits, idx, gate, dg, f, alpha, dz, s);
+    case 48: return launch_router_bwd_ep<48>(c, logits, idx, gate, dg, f, alpha, dz, s);
+    case 64: return launch_router_bwd_ep<64>(c, logits, idx, gate, dg, f, alpha, dz, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
+                          const float* dz, const void* Wg, void* dx, cudaStream_t s) {
+  const int nvec = c.d / 8;
+  bwd_dx_kernel<<<(c.T + NW - 1) / NW, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of, dz,
+                                                   static_cast<const uint4*>(Wg), c.T, c.k, c.E,
+                                                   nvec, static_cast<uint4*>(dx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
+                          float* bpart, float* dWg, float* dbias, cudaStream_t s) {
+  const int nsplit = bwd_wg_splits(c);
+  const int per = (c.T + nsplit - 1) / nsplit;
+  const int ep = (c.E + 15) / 16 * 16;
+  cudaError_t e;
+  switch (ep) {
+    case 16: e = launch_wg_ep<16>(c, dz, x, nsplit, per, part, bpart, s); break;
+    case 32: e = launch_wg_ep<32>(c, dz, x, nsplit, per, part, bpart, s); break;
+    case 48: e = launch_wg_ep<48>(c, dz, x, nsplit, per, part, bpart, s); break;
+    case 64: e = launch_wg_ep<64>(c, dz, x, nsplit, per, part, bpart, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  const int n = c.E * c.d;
+  bwd_wg_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, bpart, nsplit, c.E, c.d, dWg, dbias);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s) {
+  pad_offsets_kernel<<<1, 32, 0, s>>>(off, E, poff);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_pad(int act, const void* in, int ld_in, int C, const int32_t* off,
+                                 const int32_t* poff, int E, int64_t rp_bound, void* out,
+                                 int ld_out, cudaStream_t s) {
+  const dim3 grid((unsigned)((rp_bound + 63) / 64), (unsigned)((C + 63) / 64));
+  const __nv_bfloat16* i = static_cast<const __nv_bfloat16*>(in);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  if (act == 0) transpose_pad_kernel<0><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
+  else if (act == 1) transpose_pad_kernel<1><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
+  else transpose_pad_kernel<2><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_transpose(const void* in, int E, int A, int B, int ld_out, int a_off,
+                                    void* out, cudaStream_t s) {
+  const dim3 grid((unsigned)((B + 63) / 64), (unsigned)((A + 63) / 64), (unsigned)E);
+  weight_transpose_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(in), A, B,
+                                               ld_out, a_off, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_colsum(const void* a, int ld, int C, const int32_t* off, int E,
+                                 float* out, cudaStream_t s) {
+  const dim3 grid((unsigned)((C + 127) / 128), (unsigned)E);
+  expert_colsum_kernel<<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(a), ld, C, off,
+                                            out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -52,7 +52,9 @@ constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = UMMA_N * BK * 2;      // 32 KB
 constexpr int TMEM_COLS = 2 * UMMA_N;         // two accumulators
 
-enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2 };
+// kBwdGelu / kBwdSwiglu: the backward pass's dh = dY W2 GEMM, whose epilogue
+// multiplies by the activation's derivative at the saved pre-activations.
+enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2, kBwdGelu = 3, kBwdSwiglu = 4 };
 
 // Pipeline shape: operand stages and output staging buffers per epilogue
 // warp. Four 48 KB stages and two 2 KB buffers per warp fill the 227 KB
@@ -128,6 +130,38 @@ __device__ __forceinline__ float gelu_as(float u) {
 // overflows to +inf and the quotient is 0.
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
+// GELU'(u) = Phi(u) + u phi(u), with Phi from the same erfc approximation as
+// gelu_as (Phi(u) = 1 - q/2 for u >= 0, q/2 below) and phi(u) =
+// exp(-u^2/2) / sqrt(2 pi), which is the ex2 term already at hand.
+__device__ __forceinline__ float gelu_grad_as(float u) {
+  constexpr float kS = 0.84932180028801904f;    // sqrt(log2 e) / sqrt 2
+  constexpr float kP = 0.27273748087922250f;    // p / sqrt(log2 e), p = 0.3275911
+  constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+  const float s = fabsf(u) * kS;
+  const float t = __fdividef(1.f, fmaf(kP, s, 1.f));
+  const float e = ex2_approx(-s * s);  // exp(-u^2 / 2)
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  const float half_q = 0.5f * t * poly * e;  // erfc(|u| / sqrt 2) / 2
+  const float Phi = u >= 0.f ? 1.f - half_q : half_q;
+  return fmaf(u * kInvSqrt2Pi, e, Phi);
+}
+// sigma(u) and silu'(u) = sigma(u) (1 + u (1 - sigma(u)))
+__device__ __forceinline__ float sigmoid_f(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
+
+// Eight bf16 of a 16-byte vector to fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
 struct TileInfo {
   int e, m0, mend, n0;
 };
@@ -173,8 +207,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            const __nv_bfloat16* __restrict__ bias,
                            __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
                            const int32_t* __restrict__ o_rows,
-                           const float* __restrict__ o_scale) {
+                           const float* __restrict__ o_scale,
+                           const __nv_bfloat16* __restrict__ pre, int ldo) {
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
+  constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu;
   constexpr int STAGES = PIPE::STAGES;
   constexpr int OUT_BUFS = PIPE::OUT_BUFS;
   constexpr int BM_T = PAIR ? 2 * BM : BM;              // rows of one tile
@@ -415,7 +451,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         orow_idx = row_ok ? __ldg(o_rows + row) : 0;
         oscale = row_ok ? __ldg(o_scale + orow_idx) : 0.f;
       }
-      __nv_bfloat16* orow = out + (size_t)orow_idx * N;
       // all 32 rows of this warp belong to the tile's expert: one TMA store
       // per 32 columns; otherwise (the expert's last, partial tile, or the
       // row scatter) direct stores of the valid rows
@@ -454,10 +489,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int ch = 0; ch < OUTC / 32; ++ch) {
         const int c = cbase + 32 * ch;
         float v[32];
+        float v2[32];  // kBwdSwiglu: the second output (d up), stored N columns further
         if (MODE == kSwiglu) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             v[j] = silu_f(__uint_as_float(r[32 * ch + j])) * __uint_as_float(r[64 + 32 * ch + j]);
+        } else if (BWD) {
+          // dh for 32 columns of this row; the saved pre-activations of the
+          // same row and columns (gate a and up v for SwiGLU: v at column N + n)
+          float a[32];
+          const int col0 = ti.n0 + c;
+          const __nv_bfloat16* pr = pre + (size_t)row * (MODE == kBwdSwiglu ? 2 * N : N);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (row_ok && col0 + 8 * q + 8 <= N)
+              w = __ldg(reinterpret_cast<const uint4*>(pr + col0) + q);
+            bf16x8_to_f32(w, a + 8 * q);
+          }
+          if (MODE == kBwdGelu) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[32 * ch + j]) * gelu_grad_as(a[j]);
+          } else {
+            float u2[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 w = make_uint4(0, 0, 0, 0);
+              if (row_ok && col0 + 8 * q + 8 <= N)
+                w = __ldg(reinterpret_cast<const uint4*>(pr + N + col0) + q);
+              bf16x8_to_f32(w, u2 + 8 * q);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float dh = __uint_as_float(r[32 * ch + j]);
+              const float sg = sigmoid_f(a[j]);
+              const float sl = a[j] * sg;
+              v[j] = dh * u2[j] * sg * fmaf(a[j], 1.f - sg, 1.f);  // d gate
+              v2[j] = dh * sl;                                    // d up
+            }
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[32 * ch + j]);
@@ -476,42 +546,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= oscale;
         }
-        uint4 pk[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk[q]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            h2[j] = __floats2bfloat162_rn(v[8 * q + 2 * j], v[8 * q + 2 * j + 1]);
-        }
-        if (warp_full) {
-          // the store that last used this buffer (OUT_BUFS stores ago) must
-          // have read it
-          uint8_t* my_out = my_out0 + (n_stores % OUT_BUFS) * STAGE_OUT_BYTES;
-          ++n_stores;
-          if (lane == 0) {
-            if (OUT_BUFS == 1) bulk_wait_read0();
-            else bulk_wait_read<OUT_BUFS - 1>();
-          }
-          __syncwarp();
-          // 64-byte swizzle (the layout of the store's tensor map): 16-byte
-          // chunk q of row r sits at chunk q ^ ((r >> 1) & 3), so the 32
-          // rows' writes of one chunk hit all 32 banks (4 wavefronts, not 16)
-          uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
-          const int sw = (lane >> 1) & 3;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q ^ sw] = pk[q];
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmOut, my_out, ti.n0 + c, wrow0);
-            bulk_commit();
-          }
-        } else if (row_ok) {
+        for (int o = 0; o < (MODE == kBwdSwiglu ? 2 : 1); ++o) {
+          const float* vv = o == 0 ? v : v2;
+          const int ocol = ti.n0 + c + o * N;  // first output column of this chunk
+          uint4 pk[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int col = ti.n0 + c + 8 * q;
-            if (col + 8 <= N) *reinterpret_cast<uint4*>(orow + col) = pk[q];
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk[q]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              h2[j] = __floats2bfloat162_rn(vv[8 * q + 2 * j], vv[8 * q + 2 * j + 1]);
+          }
+          if (warp_full && ti.n0 + c + 32 <= N) {
+            // the store that last used this buffer (OUT_BUFS stores ago) must
+            // have read it
+            uint8_t* my_out = my_out0 + (n_stores % OUT_BUFS) * STAGE_OUT_BYTES;
+            ++n_stores;
+            if (lane == 0) {
+              if (OUT_BUFS == 1) bulk_wait_read0();
+              else bulk_wait_read<OUT_BUFS - 1>();
+            }
+            __syncwarp();
+            // 64-byte swizzle (the layout of the store's tensor map): 16-byte
+            // chunk q of row r sits at chunk q ^ ((r >> 1) & 3), so the 32
+            // rows' writes of one chunk hit all 32 banks (4 wavefronts, not 16)
+            uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q ^ sw] = pk[q];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, my_out, ocol, wrow0);
+              bulk_commit();
+            }
+          } else if (row_ok) {
+            __nv_bfloat16* orow2 = out + (size_t)orow_idx * ldo;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int col = ti.n0 + c + 8 * q;
+              if (col + 8 <= N) *reinterpret_cast<uint4*>(orow2 + col + o * N) = pk[q];
+            }
           }
         }
       }
@@ -561,11 +637,11 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 [rows, K] row-major, box [128 rows, 64 cols], 128-byte swizzle.
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint64_t ld = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t gdim[2] = {K, rows};
-  cuuint64_t gstride[1] = {K * 2};
+  cuuint64_t gstride[1] = {(ld ? ld : K) * 2};
   cuuint32_t box[2] = {BK, BM};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
@@ -589,11 +665,12 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint6
 
 // 2-D bf16 [rows, N] row-major, box [32 rows, 32 cols], no swizzle: the
 // epilogue's output blocks.
-bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows) {
+bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows,
+                  uint64_t ld = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t gdim[2] = {N, rows};
-  cuuint64_t gstride[1] = {N * 2};
+  cuuint64_t gstride[1] = {(ld ? ld : N) * 2};
   cuuint32_t box[2] = {32, 32};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
@@ -605,7 +682,8 @@ template <int MODE, bool SCATTER, bool PAIR, class PIPE>
 cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                           const CUtensorMap& o, const int32_t* offset, int E, int N, int K,
                           const void* bias, void* out, int64_t rows_bound, int32_t* hdr,
-                          const int32_t* o_rows, const float* o_scale, cudaStream_t s) {
+                          const int32_t* o_rows, const float* o_scale, const void* pre,
+                          int ldo, cudaStream_t s) {
   constexpr size_t SMEM_BYTES = smem_bytes<PAIR, PIPE>();
   auto kernel = grouped_gemm_tc_kernel<MODE, SCATTER, PAIR, PIPE>;
   static int max_units[64] = {};  // per device: CTAs (or CTA pairs) resident at once
@@ -643,7 +721,8 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   const unsigned grid = (unsigned)(PAIR ? 2 * units : units);
   return launch_pdl_cluster(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
                             b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
-                            static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale);
+                            static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale,
+                            static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N);
 }
 
 template <int MODE, bool SCATTER>
@@ -651,12 +730,13 @@ cudaError_t launch_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& b3, const CUtensorMap& o, const int32_t* offset, int E,
                         int N, int K, const void* bias, void* out, int64_t rows_bound,
                         int32_t* hdr, const int32_t* o_rows, const float* o_scale,
-                        cudaStream_t s) {
+                        cudaStream_t s, const void* pre = nullptr, int ldo = 0) {
   if (pair)
     return launch_gemm_p<MODE, SCATTER, true, PipePairShape>(
-        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, s);
+        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, s);
   return launch_gemm_p<MODE, SCATTER, false, PipeShape>(a, b, b3, o, offset, E, N, K, bias, out,
-                                                        rows_bound, hdr, o_rows, o_scale, s);
+                                                        rows_bound, hdr, o_rows, o_scale, pre,
+                                                        ldo, s);
 }
 
 }  // namespace
@@ -739,6 +819,58 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
                                      rows_bound, hdr, fz->scatter_rows, fz->scatter_scale, s);
   return launch_gemm<kPlain, false>(pair, mh, mw2, mw2, moy, offset, c.E, c.d, c.H, b2e, Y,
                                     rows_bound, hdr, nullptr, nullptr, s);
+}
+
+// Expert part of the backward pass (tensor cores, bf16):
+//   pre  = xd W1^T (+ b1) [R, H]      (SwiGLU: [a | v] = xd [W1; W3]^T, [R, 2H])
+//   dact = (dY W2) * act'(pre)        [R, H]  (SwiGLU: [d gate | d up], [R, 2H])
+//   dxd  = dact W1                    [R, d]  (SwiGLU: [d gate | d up] [W1; W3])
+// W2T [E, H, d] and W13T [E, d, Hp] (Hp = H or 2H) are the transposed expert
+// weights (K-major operands); the pre-activations are recomputed here rather
+// than kept from the forward pass.
+cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
+                              const void* W1, const void* W3, const void* b1, const void* W2T,
+                              const void* W13T, const void* dY, void* pre, void* dact,
+                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
+  const uint64_t R = (uint64_t)rows_bound;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  const bool pair = use_pairs(c);
+  const uint64_t H = (uint64_t)c.H, d = (uint64_t)c.d, Hp = swiglu ? 2 * H : H;
+  const uint32_t box = pair ? 128 : UMMA_N;
+  CUtensorMap mxd, mw1, mw3, mpa, mpv, mdy, mw2t, mdact_o, mdact_a, mw13t, mdxd;
+  if (!make_map_2d(&mxd, xd, d, R) || !make_map_3d(&mw1, W1, d, H, c.E, box) ||
+      !make_map_out(&mpa, pre, H, R, Hp) || !make_map_2d(&mdy, dY, d, R) ||
+      !make_map_3d(&mw2t, W2T, d, H, c.E, box) || !make_map_out(&mdact_o, dact, Hp, R) ||
+      !make_map_2d(&mdact_a, dact, Hp, R) || !make_map_3d(&mw13t, W13T, Hp, d, c.E, box) ||
+      !make_map_out(&mdxd, dxd, d, R))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  // recomputed pre-activations
+  e = launch_gemm<kPlain, false>(pair, mxd, mw1, mw1, mpa, offset, c.E, c.H, c.d,
+                                 swiglu ? nullptr : b1, pre, rows_bound, hdr, nullptr, nullptr, s,
+                                 nullptr, (int)Hp);
+  if (e != cudaSuccess) return e;
+  if (swiglu) {
+    if (!make_map_3d(&mw3, W3, d, H, c.E, box) ||
+        !make_map_out(&mpv, static_cast<__nv_bfloat16*>(pre) + H, H, R, Hp))
+      return cudaErrorInvalidValue;
+    e = launch_gemm<kPlain, false>(pair, mxd, mw3, mw3, mpv, offset, c.E, c.H, c.d, nullptr,
+                                   static_cast<__nv_bfloat16*>(pre) + H, rows_bound, hdr, nullptr,
+                                   nullptr, s, nullptr, (int)Hp);
+    if (e != cudaSuccess) return e;
+  }
+  // dh = dY W2, times the activation's derivative
+  if (swiglu)
+    e = launch_gemm<kBwdSwiglu, false>(pair, mdy, mw2t, mw2t, mdact_o, offset, c.E, c.H, c.d,
+                                       nullptr, dact, rows_bound, hdr, nullptr, nullptr, s, pre,
+                                       (int)Hp);
+  else
+    e = launch_gemm<kBwdGelu, false>(pair, mdy, mw2t, mw2t, mdact_o, offset, c.E, c.H, c.d,
+                                     nullptr, dact, rows_bound, hdr, nullptr, nullptr, s, pre);
+  if (e != cudaSuccess) return e;
+  // dxd = dact [W1; W3]
+  return launch_gemm<kPlain, false>(pair, mdact_a, mw13t, mw13t, mdxd, offset, c.E, c.d,
+                                    (int)Hp, nullptr, dxd, rows_bound, hdr, nullptr, nullptr, s);
 }
 
 }  // namespace moe

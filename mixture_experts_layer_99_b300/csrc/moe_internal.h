@@ -197,6 +197,34 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* 
                            const float* gate, void* y, cudaStream_t s,
                            const void* base = nullptr);
 cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s);
+
+// ---- backward pass
+cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
+                              const void* W1, const void* W3, const void* b1, const void* W2T,
+                              const void* W13T, const void* dY, void* pre, void* dact,
+                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s);
+cudaError_t launch_wgrad_tc(const void* At, const void* Bt, int64_t ld, const int32_t* poff,
+                            int E, int M, int N, int m_split, float* out, float* out2,
+                            int32_t* hdr, cudaStream_t s);
+int bwd_wg_splits(const moe_config_t& c);
+cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
+                               const int32_t* slot_of, const float* gate, void* dY, float* dg,
+                               cudaStream_t s);
+cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
+                              const float* gate, const float* dg, const float* f, float alpha,
+                              float* dz, cudaStream_t s);
+cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
+                          const float* dz, const void* Wg, void* dx, cudaStream_t s);
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
+                          float* bpart, float* dWg, float* dbias, cudaStream_t s);
+cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s);
+cudaError_t launch_transpose_pad(int act, const void* in, int ld_in, int C, const int32_t* off,
+                                 const int32_t* poff, int E, int64_t rp_bound, void* out,
+                                 int ld_out, cudaStream_t s);
+cudaError_t launch_weight_transpose(const void* in, int E, int A, int B, int ld_out, int a_off,
+                                    void* out, cudaStream_t s);
+cudaError_t launch_expert_colsum(const void* a, int ld, int C, const int32_t* off, int E,
+                                 float* out, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,
                        const float* partial, int nparts, float* f, float* P, float* L,
                        int32_t* dropped, cudaStream_t s);

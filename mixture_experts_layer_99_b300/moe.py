@@ -30,7 +30,8 @@ EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspa
             "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
             "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
             "moe_layer_forward_launch_count", "moe_layer_forward_profiled",
-            "moe_workspace_size_shared", "moe_layer_forward_shared", "moe_dispatch_static_scratch"]
+            "moe_workspace_size_shared", "moe_layer_forward_shared", "moe_dispatch_static_scratch",
+            "moe_workspace_size_backward", "moe_layer_backward"]
 
 
 class MoEError(RuntimeError):
@@ -66,6 +67,11 @@ class LayerOutputs(ctypes.Structure):
                 ("topk_gate", c_void_p), ("slot_of", c_void_p), ("expert_count", c_void_p),
                 ("expert_offset", c_void_p), ("f", c_void_p), ("P", c_void_p),
                 ("L_balance", c_void_p), ("dropped", c_void_p)]
+
+
+class LayerGrads(ctypes.Structure):
+    _fields_ = [("dx", c_void_p), ("dWg", c_void_p), ("dbias", c_void_p), ("dW1", c_void_p),
+                ("dW3", c_void_p), ("dW2", c_void_p), ("db1", c_void_p), ("db2", c_void_p)]
 
 
 _LIB = None
@@ -107,6 +113,10 @@ def lib():
                                                  POINTER(c_void_p)]),
         "moe_layer_forward_host": (c_int32, [cfgp, vp, POINTER(LayerInputs), vp, vp, vp,
                                              c_size_t, vp]),
+        "moe_workspace_size_backward": (c_int32, [cfgp, POINTER(c_size_t)]),
+        "moe_layer_backward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs), vp,
+                                         ctypes.c_float, POINTER(LayerGrads), vp, c_size_t, vp,
+                                         c_size_t, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -391,3 +401,52 @@ def layer_forward_host(cfg, x_host, weights: dict, y_host, *, ws, L_host=None):
     _need(y_host, "y_host", _dt(cfg), (cfg.T, cfg.d), torch.device("cpu"))
     _call("moe_layer_forward_host", ctypes.byref(cfg), _ptr(x_host), ctypes.byref(li),
           _ptr(y_host), _ptr(L_host), _ptr(ws), ws.numel(), _stream(dev))
+
+
+def workspace_backward(cfg: Config, device="cuda") -> torch.Tensor:
+    """The backward pass's own workspace (256-byte aligned, header zeroed)."""
+    n = c_size_t(0)
+    _call("moe_workspace_size_backward", ctypes.byref(cfg), ctypes.byref(n))
+    ws = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n.value]
+    _call("moe_workspace_init", c_void_p(ws.data_ptr()), n.value,
+          c_void_p(_stream(ws.device)))
+    return ws
+
+
+def alloc_grads(cfg, inp: dict, device):
+    """Gradient buffers matching the inputs: dx in the layer dtype, fp32 weight
+    gradients; dbias, dW3, db1, db2 only where the inputs have them."""
+    E, d, H, T = cfg.E, cfg.d, cfg.H, cfg.T
+    f32 = dict(dtype=torch.float32, device=device)
+    g = dict(dx=torch.empty(T, d, dtype=_dt(cfg), device=device),
+             dWg=torch.empty(E, d, **f32), dW1=torch.empty(E, H, d, **f32),
+             dW2=torch.empty(E, d, H, **f32))
+    if inp.get("bias") is not None:
+        g["dbias"] = torch.empty(E, **f32)
+    if inp.get("W3") is not None:
+        g["dW3"] = torch.empty(E, H, d, **f32)
+    if inp.get("b1") is not None:
+        g["db1"] = torch.empty(E, H, **f32)
+    if inp.get("b2") is not None:
+        g["db2"] = torch.empty(E, d, **f32)
+    return g
+
+
+def layer_backward(cfg, inp: dict, fwd: dict, dy, alpha: float = 0.0, *, ws, bws=None,
+                   grads: Optional[dict] = None):
+    """Gradients of sum <dy, y> + alpha * L_balance for the forward call that
+    produced ``fwd`` (the output dict of layer_forward with full=True) with
+    workspace ``ws``. Returns the gradient dict (see alloc_grads)."""
+    dev = inp["x"].device
+    li = _layer_inputs(cfg, inp, dev)
+    _need(dy, "dy", _dt(cfg), (cfg.T, cfg.d), dev)
+    lo = LayerOutputs(*[_ptr(fwd.get(n)) for n, _ in LayerOutputs._fields_])
+    g = alloc_grads(cfg, inp, dev) if grads is None else grads
+    lg = LayerGrads(*[_ptr(g.get(n)) for n, _ in LayerGrads._fields_])
+    bws = workspace_backward(cfg, dev) if bws is None else bws
+    _call("moe_layer_backward", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(lo),
+          _ptr(dy), ctypes.c_float(alpha), ctypes.byref(lg), _ptr(ws), ws.numel(), _ptr(bws),
+          bws.numel(), _stream(dev))
+    return g

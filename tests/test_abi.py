@@ -160,3 +160,27 @@ def test_shared_expert_validation():
                                           need.value, None) == 1
     assert L.moe_layer_forward_shared(r, ctypes.byref(inp), ctypes.byref(ok), ctypes.byref(out),
                                       ctypes.c_void_p(4096), need.value - 1, None) == 3
+
+
+def test_backward_validation_without_a_gpu():
+    """The backward's host-side checks: unsupported shapes and missing
+    pointers are refused before anything is enqueued."""
+    from mixture_experts_layer_99_b300 import workloads as W
+    L = moe.lib()
+    n = ctypes.c_size_t(0)
+    # fp32 and E > 64 have no backward (UNSUPPORTED = 2)
+    assert L.moe_workspace_size_backward(ctypes.byref(moe.config_from_workload(
+        W.WORKLOADS["ref_fp32"])), ctypes.byref(n)) == 2
+    big = W.small(W.WORKLOADS["switch_top1"], T=64, d=64, H=64, E=128, k=2)
+    assert L.moe_workspace_size_backward(ctypes.byref(moe.config_from_workload(big)),
+                                         ctypes.byref(n)) == 2
+    cfg = moe.config_from_workload(W.WORKLOADS["switch_top1"])
+    assert L.moe_workspace_size_backward(ctypes.byref(cfg), ctypes.byref(n)) == 0
+    assert n.value > 0
+    li = moe.LayerInputs()
+    lo = moe.LayerOutputs()
+    lg = moe.LayerGrads()
+    # missing inputs, outputs and gradients: INVALID_ARG (1)
+    assert L.moe_layer_backward(ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(lo), None,
+                                ctypes.c_float(0.0), ctypes.byref(lg), None, 0, None, 0,
+                                None) == 1

@@ -1,0 +1,109 @@
+"""Parity of moe_layer_backward (the C-ABI backward call) with the fp64
+backward oracle on the same seeded inputs, routing taken from the GPU's own
+fp32 logits. Every gradient is compared on every element."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_99_b300 import moe, workloads as W
+from oracle import moe_backward as OB
+from parity_util import np_of, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+WL = W.WORKLOADS
+
+# max |err| / max |ref| per gradient. The GPU path rounds dY, the recomputed
+# pre-activations, the activation gradients, dxd and the transposed operands
+# to bf16 (relative spacing 2^-8) and accumulates in fp32; each gradient is a
+# sum of such products, so a few bf16 ulps of the largest entry bound it.
+TOL = dict(dx=2e-2, dWg=2e-2, dbias=2e-2, dW1=2e-2, dW3=2e-2, dW2=2e-2, db1=2e-2, db2=2e-2)
+
+CASES = {
+    "switch_small": (W.small(WL["switch_top1"], T=1500, d=256, H=512), 0.1, True),
+    "switch_pairs": (W.small(WL["switch_top1"], T=4100, d=256, H=512, E=4), 0.1, False),
+    "mixtral_small": (W.small(WL["mixtral"], T=700, d=256, H=384), 0.05, False),
+    "mixtral_pairs": (W.small(WL["mixtral"], T=2100, d=256, H=384, E=4), 0.05, False),
+    "longtail_small": (W.small(WL["longtail"], T=2000, d=128, H=192), 0.01, False),
+    "sweep_small": (W.small(WL["sweep_e16_k4"], T=2048, d=256, H=512), 0.1, True),
+    "drops_heavy": (W.small(WL["longtail"], T=999, d=64, H=64, c=Fraction(1, 3)), 0.2, False),
+    "ragged_dims": (W.small(WL["switch_top1"], T=600, d=136, H=200, E=5, k=2), 0.3, True),
+}
+
+
+def _run(w, alpha, with_bias, seed=0):
+    inp = W.make_inputs(w, seed)
+    if with_bias:  # nonzero expert biases for the GELU bias gradients
+        g = torch.Generator().manual_seed(seed + 99)
+        inp["b1"] = (0.1 * torch.randn(w.E, w.H, generator=g)).to(w.torch_dtype)
+        inp["b2"] = (0.1 * torch.randn(w.E, w.d, generator=g)).to(w.torch_dtype)
+    gdy = torch.Generator().manual_seed(seed + 7)
+    dy = torch.randn(w.T, w.d, generator=gdy).to(w.torch_dtype)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(inp, DEV)
+    ws = moe.workspace(cfg, DEV)
+    out = moe.layer_forward(cfg, dinp, ws=ws)
+    grads = moe.layer_backward(cfg, dinp, out, dy.to(DEV), alpha, ws=ws)
+    torch.cuda.synchronize()
+    return inp, dy, cfg, out, grads
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_backward_matches_oracle(name):
+    w, alpha, with_bias = CASES[name]
+    inp, dy, cfg, out, grads = _run(w, alpha, with_bias)
+    ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, alpha, w.tau,
+                          logits=out["logits"].cpu().numpy())
+    # the oracle followed the GPU's routing
+    np.testing.assert_array_equal(ref["route"]["slot_of"], out["slot_of"].cpu().numpy())
+    pairs = dict(dx=ref["dx"], dWg=ref["dWg"], dbias=ref["dbias"], dW1=ref["dW1"],
+                 dW3=ref["dW3"], dW2=ref["dW2"], db1=ref["db1"], db2=ref["db2"])
+    errs = {}
+    for key, r in pairs.items():
+        if r is None:
+            assert grads.get(key) is None, key
+            continue
+        errs[key] = rel_err(np_of(grads[key]), r)
+    print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    for key, e in errs.items():
+        assert e <= TOL[key], (key, e)
+
+
+def test_backward_is_deterministic():
+    w = W.small(WL["mixtral"], T=900, d=128, H=192)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(W.make_inputs(w), DEV)
+    dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(3)).to(w.torch_dtype).to(DEV)
+    ws = moe.workspace(cfg, DEV)
+    out = moe.layer_forward(cfg, dinp, ws=ws)
+    a = moe.layer_backward(cfg, dinp, out, dy, 0.1, ws=ws)
+    b = moe.layer_backward(cfg, dinp, out, dy, 0.1, ws=ws)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_backward_status_is_clean():
+    w = W.small(WL["switch_top1"], T=512, d=128, H=256)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(W.make_inputs(w), DEV)
+    ws = moe.workspace(cfg, DEV)
+    out = moe.layer_forward(cfg, dinp, ws=ws)
+    bws = moe.workspace_backward(cfg, DEV)
+    dy = torch.ones(w.T, w.d, dtype=torch.bfloat16, device=DEV)
+    moe.layer_backward(cfg, dinp, out, dy, 0.0, ws=ws, bws=bws)
+    assert moe.device_status(bws) == (0, 0)
+
+
+@pytest.mark.slow
+def test_backward_full_size_switch():
+    """switch_top1 at full size: dWg, dx and the expert gradients on every
+    element (the oracle's fp64 run takes tens of seconds)."""
+    w = WL["switch_top1"]
+    inp, dy, cfg, out, grads = _run(w, 0.01, False)
+    ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, 0.01, w.tau,
+                          logits=out["logits"].cpu().numpy())
+    for key in ("dx", "dWg", "dW1", "dW2"):
+        assert rel_err(np_of(grads[key]), ref[key]) <= TOL[key], key
