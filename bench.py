@@ -164,6 +164,35 @@ def footprint_bytes(inp):
     return sum(v.numel() * v.element_size() for v in inp.values() if v is not None)
 
 
+def time_backward(w, cfg, inp, ws, stream, dev, kept, reps):
+    """ms per moe_layer_backward call (loss = sum <dy, y> + 0.01 L_balance),
+    and the tensor-core GEMM work it executes: the recomputed
+    pre-activations, dh = dY W2, dxd = dact [W1; W3] and the weight
+    gradients, kept * 2 * d * H * (3 (nm - 1) + 2) flops."""
+    from mixture_experts_layer_99_b300 import moe
+    out = moe.alloc_outputs(cfg, dev)
+    moe.layer_forward(cfg, inp, ws=ws, out=out)
+    dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(5)).to(
+        w.torch_dtype).to(dev)
+    bws = moe.workspace_backward(cfg, dev)
+    grads = moe.alloc_grads(cfg, inp, dev)
+    for _ in range(2):
+        moe.layer_backward(cfg, inp, out, dy, 0.01, ws=ws, bws=bws, grads=grads)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        moe.layer_backward(cfg, inp, out, dy, 0.01, ws=ws, bws=bws, grads=grads)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / reps
+    flops = kept * 2 * w.d * w.H * (3 * (w.nmat - 1) + 2)
+    return dict(ms_per_call=ms, calls=reps, gemm_tflops_executed=flops / (ms / 1e3) / 1e12,
+                tokens_per_s=w.T / (ms / 1e3), loss="sum <dy, y> + 0.01 L_balance",
+                note="eager calls on one input set; GEMM work includes the recomputed "
+                     "pre-activations")
+
+
 def traffic_record(kernel_src_sha, workload):
     """The committed ncu DRAM traffic of the grouped GEMM, if it was taken on
     this workload from the current kernel source."""
@@ -426,6 +455,12 @@ def main():
                 frac_of_sustained=(achieved / peaks["bf16_tflops_sustained"]
                                    if peaks.get("bf16_tflops_sustained") else None))
 
+    # ---- backward pass of the same layer call (moe_layer_backward), timed
+    # alone with CUDA events after one forward call that left its state in ws
+    bwd = None
+    if w.dtype == "bf16" and w.E <= 64 and w.shared_H == 0:
+        bwd = time_backward(w, cfg, sets[0], ws, stream, dev, kept, max(3, args.steps // 20))
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = time_oracle(w)
@@ -464,6 +499,7 @@ def main():
                 note="stage times from moe_layer_forward_profiled events; for k = 1 the "
                      "combine runs inside GEMM2"),
             device_status=status[0],
+            backward=bwd,
         )
         print(json.dumps(line), flush=True)
     if pg:

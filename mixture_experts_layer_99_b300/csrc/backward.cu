@@ -133,35 +133,57 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     if (e < E) dz[(size_t)t * E + e] = p[e] * (dp[e] - pdp) * inv_tau;
 }
 
-// One warp per token: dx_t = sum over kept slots of dxd[slot] (slot order)
-// + sum_e dz[t, e] Wg[e, :] (expert order), fp32, rounded once.
-__global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dxd,
-                                                    const int32_t* __restrict__ slot_of,
-                                                    const float* __restrict__ dz,
-                                                    const uint4* __restrict__ Wg, int T, int k,
-                                                    int E, int nvec, uint4* __restrict__ dx) {
-  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int lane = threadIdx.x & 31;
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int sl = slot_of[(size_t)t * k + j];
-      if (sl < 0) continue;
-      float a[8];
-      unpack8(__ldg(dxd + (size_t)sl * nvec + v), a);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += a[i];
-    }
-    for (int e = 0; e < E; ++e) {
-      const float z = __ldg(dz + (size_t)t * E + e);
-      float w[8];
-      unpack8(__ldg(Wg + (size_t)e * nvec + v), w);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(z, w[i], acc[i]);
-    }
-    dx[(size_t)t * nvec + v] = pack8(acc);
+// dx_t = sum over the kept slots of dxd[slot] (slot order) + sum_e dz[t, e]
+// Wg[e, :] (a fixed order of the experts), fp32, rounded once. Block = 32 tokens x 256
+// columns: thread c owns one column for the 32 tokens; the block's Wg columns
+// and dz rows are staged in shared memory.
+constexpr int DX_TOK = 32, DX_COLS = 256;
+template <int EP>
+__global__ void __launch_bounds__(DX_COLS) bwd_dx_kernel(const __nv_bfloat16* __restrict__ dxd,
+                                                         const int32_t* __restrict__ slot_of,
+                                                         const float* __restrict__ dz,
+                                                         const __nv_bfloat16* __restrict__ Wg,
+                                                         int T, int k, int E, int d,
+                                                         __nv_bfloat16* __restrict__ dx) {
+  __shared__ __align__(16) float sdz[DX_TOK][EP];
+  __shared__ __nv_bfloat16 swg[EP][DX_COLS];  // <= 32 KB (static shared memory stays < 48 KB)
+  const int c = blockIdx.x * DX_COLS + threadIdx.x;
+  const int t0 = blockIdx.y * DX_TOK;
+  for (int i = threadIdx.x; i < DX_TOK * EP; i += DX_COLS) {
+    const int t = t0 + i / EP, e = i % EP;
+    sdz[i / EP][e] = (t < T && e < E) ? dz[(size_t)t * E + e] : 0.f;
   }
+#pragma unroll 4
+  for (int e = 0; e < EP; ++e)
+    swg[e][threadIdx.x] = (e < E && c < d) ? Wg[(size_t)e * d + c] : __float2bfloat16_rn(0.f);
+  __syncthreads();
+  if (c >= d) return;
+  float acc[DX_TOK];
+#pragma unroll
+  for (int t = 0; t < DX_TOK; ++t) acc[t] = 0.f;
+  for (int j = 0; j < k; ++j) {
+#pragma unroll 8
+    for (int t = 0; t < DX_TOK; ++t) {
+      if (t0 + t >= T) continue;
+      const int sl = slot_of[(size_t)(t0 + t) * k + j];
+      if (sl >= 0) acc[t] += __bfloat162float(dxd[(size_t)sl * d + c]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < EP; e += 4) {
+    const float w0 = __bfloat162float(swg[e][threadIdx.x]);
+    const float w1 = __bfloat162float(swg[e + 1][threadIdx.x]);
+    const float w2 = __bfloat162float(swg[e + 2][threadIdx.x]);
+    const float w3 = __bfloat162float(swg[e + 3][threadIdx.x]);
+#pragma unroll
+    for (int t = 0; t < DX_TOK; ++t) {
+      const float4 z = *reinterpret_cast<const float4*>(&sdz[t][e]);
+      acc[t] = fmaf(z.x, w0, fmaf(z.y, w1, fmaf(z.z, w2, fmaf(z.w, w3, acc[t]))));
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < DX_TOK; ++t)
+    if (t0 + t < T) dx[(size_t)(t0 + t) * d + c] = __float2bfloat16_rn(acc[t]);
 }
 
 // dWg = dz^T x and db = sum_t dz: block (column block cb, token split sp)
@@ -172,7 +194,8 @@ template <int EP>
 __global__ void __launch_bounds__(WG_COLS) bwd_wg_partial_kernel(
     const float* __restrict__ dz, const __nv_bfloat16* __restrict__ x, int T, int d, int E,
     int tok_per_split, float* __restrict__ part, float* __restrict__ bpart) {
-  __shared__ float sdz[WG_TOK][EP];
+  __shared__ __align__(16) float sdz[WG_TOK][EP];
+  __shared__ float sx[WG_TOK][WG_COLS];
   const int c = blockIdx.x * WG_COLS + threadIdx.x;
   const int sp = blockIdx.y;
   const int t0 = sp * tok_per_split;
@@ -187,12 +210,23 @@ __global__ void __launch_bounds__(WG_COLS) bwd_wg_partial_kernel(
       const int tt = tb + i / EP, e = i % EP;
       sdz[i / EP][e] = (tt < t1 && e < E) ? dz[(size_t)tt * E + e] : 0.f;
     }
+    // this thread's column of the batch's tokens, all loads in flight at once
+#pragma unroll 8
+    for (int i = 0; i < WG_TOK; ++i)
+      sx[i][threadIdx.x] =
+          (tb + i < t1 && c < d) ? __bfloat162float(x[(size_t)(tb + i) * d + c]) : 0.f;
     __syncthreads();
-    const int n = min(WG_TOK, t1 - tb);
-    for (int i = 0; i < n; ++i) {
-      const float xv = c < d ? __bfloat162float(x[(size_t)(tb + i) * d + c]) : 0.f;
+#pragma unroll 4
+    for (int i = 0; i < WG_TOK; ++i) {
+      const float xv = sx[i][threadIdx.x];
 #pragma unroll
-      for (int e = 0; e < EP; ++e) acc[e] = fmaf(sdz[i][e], xv, acc[e]);
+      for (int e = 0; e < EP; e += 4) {
+        const float4 z = *reinterpret_cast<const float4*>(&sdz[i][e]);
+        acc[e] = fmaf(z.x, xv, acc[e]);
+        acc[e + 1] = fmaf(z.y, xv, acc[e + 1]);
+        acc[e + 2] = fmaf(z.z, xv, acc[e + 2]);
+        acc[e + 3] = fmaf(z.w, xv, acc[e + 3]);
+      }
       if (threadIdx.x < EP) bacc += sdz[i][threadIdx.x];
     }
   }
@@ -240,13 +274,14 @@ __global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int E,
 // poff_e + (r - off_e); the columns up to the next multiple of 64 are zero.
 // ACT 0: copy of in[:, c]; 1: gelu(in[:, c]); 2: silu(in[:, c]) * in[:, C + c]
 // (the SwiGLU hidden row from the packed [gate | up] pre-activations).
-// Block = 64 padded columns x 64 channels; a 64-column block never straddles
-// two experts because every poff_e is a multiple of 64.
+// Block = 64 padded columns x 64 channels, moved as 16-byte vectors (C, the
+// strides and the channel offsets are multiples of 8); a 64-column block
+// never straddles two experts because every poff_e is a multiple of 64.
 template <int ACT>
 __global__ void __launch_bounds__(256) transpose_pad_kernel(
     const __nv_bfloat16* __restrict__ in, int ld_in, int C, const int32_t* __restrict__ off,
     const int32_t* __restrict__ poff, int E, __nv_bfloat16* __restrict__ out, int ld_out) {
-  __shared__ float tile[64][65];
+  __shared__ __align__(16) __nv_bfloat16 tile[64][72];  // [row i][channel j]
   const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
   if (p0 >= poff[E]) return;
   int lo = 0, hi = E - 1;  // expert with poff_e <= p0 < poff_{e+1}
@@ -259,50 +294,70 @@ __global__ void __launch_bounds__(256) transpose_pad_kernel(
   const int local = p0 - poff[e];
   const int nvalid = min(64, off[e + 1] - off[e] - local);
   const int r0 = off[e] + local;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
-  for (int i = ty; i < 64; i += 4) {
-    float v = 0.f;
-    const int c = c0 + tx;
+  const int tid = threadIdx.x;
+  // load: 64 rows x 8 vectors of 8 channels
+  for (int q = tid; q < 64 * 8; q += 256) {
+    const int i = q >> 3, jv = q & 7;
+    const int c = c0 + jv * 8;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (i < nvalid && c < C) {
       const __nv_bfloat16* rp = in + (size_t)(r0 + i) * ld_in;
-      const float a = __bfloat162float(rp[c]);
-      if (ACT == 0) {
-        v = a;
-      } else if (ACT == 1) {
-        v = 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
-      } else {
-        const float u = __bfloat162float(rp[C + c]);
-        v = a / (1.f + expf(-a)) * u;
+      unpack8(__ldg(reinterpret_cast<const uint4*>(rp + c)), v);
+      if (ACT == 1) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = 0.5f * v[t] * (1.f + erff(v[t] * 0.70710678118654752f));
+      } else if (ACT == 2) {
+        float u[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(rp + C + c)), u);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = v[t] / (1.f + expf(-v[t])) * u[t];
       }
     }
-    tile[i][tx] = v;
+    *reinterpret_cast<uint4*>(&tile[i][jv * 8]) = pack8(v);
   }
   __syncthreads();
-  for (int i = ty; i < 64; i += 4) {
-    const int c = c0 + i;
-    if (c < C) out[(size_t)c * ld_out + p0 + tx] = __float2bfloat16_rn(tile[tx][i]);
+  // store: channel j, 8 consecutive padded columns per 16-byte vector
+  for (int q = tid; q < 64 * 8; q += 256) {
+    const int j = q & 63, iv = q >> 6;
+    const int c = c0 + j;
+    if (c >= C) continue;
+    uint4 w;
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&w);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) h[t] = tile[iv * 8 + t][j];
+    *reinterpret_cast<uint4*>(out + (size_t)c * ld_out + p0 + iv * 8) = w;
   }
 }
 
 // Batched transpose of expert weights: out[e][b][a + a_off] = in[e][a][b]
-// (in [E, A, B] row-major, out [E, B, ld_out]).
+// (in [E, A, B] row-major, out [E, B, ld_out]); 64 x 64 tiles moved as
+// 16-byte vectors (A, B, ld_out and a_off are multiples of 8).
 __global__ void __launch_bounds__(256) weight_transpose_kernel(
     const __nv_bfloat16* __restrict__ in, int A, int B, int ld_out, int a_off,
     __nv_bfloat16* __restrict__ out) {
-  __shared__ __nv_bfloat16 tile[64][66];
+  __shared__ __align__(16) __nv_bfloat16 tile[64][72];  // [a][b]
   const int e = blockIdx.z;
   const int a0 = blockIdx.y * 64, b0 = blockIdx.x * 64;
   const __nv_bfloat16* ie = in + (size_t)e * A * B;
   __nv_bfloat16* oe = out + (size_t)e * B * ld_out;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-  for (int i = ty; i < 64; i += 4) {
-    const int a = a0 + i, b = b0 + tx;
-    tile[i][tx] = (a < A && b < B) ? ie[(size_t)a * B + b] : __float2bfloat16_rn(0.f);
+  const int tid = threadIdx.x;
+  for (int q = tid; q < 64 * 8; q += 256) {
+    const int i = q >> 3, jv = q & 7;
+    const int a = a0 + i, b = b0 + jv * 8;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (a < A && b < B) w = __ldg(reinterpret_cast<const uint4*>(ie + (size_t)a * B + b));
+    *reinterpret_cast<uint4*>(&tile[i][jv * 8]) = w;
   }
   __syncthreads();
-  for (int i = ty; i < 64; i += 4) {
-    const int b = b0 + i, a = a0 + tx;
-    if (a < A && b < B) oe[(size_t)b * ld_out + a_off + a] = tile[tx][i];
+  for (int q = tid; q < 64 * 8; q += 256) {
+    const int j = q & 63, iv = q >> 6;
+    const int b = b0 + j, a = a0 + iv * 8;
+    if (b >= B || a >= A) continue;
+    uint4 w;
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&w);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) h[t] = tile[iv * 8 + t][j];
+    *reinterpret_cast<uint4*>(oe + (size_t)b * ld_out + a_off + a) = w;
   }
 }
 
@@ -369,13 +424,25 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
   }
 }
 
+template <int EP>
+cudaError_t launch_dx_ep(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
+                         const float* dz, const void* Wg, void* dx, cudaStream_t s) {
+  const dim3 grid((unsigned)((c.d + DX_COLS - 1) / DX_COLS), (unsigned)((c.T + DX_TOK - 1) / DX_TOK));
+  bwd_dx_kernel<EP><<<grid, DX_COLS, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dxd), slot_of, dz, static_cast<const __nv_bfloat16*>(Wg),
+      c.T, c.k, c.E, c.d, static_cast<__nv_bfloat16*>(dx));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
                           const float* dz, const void* Wg, void* dx, cudaStream_t s) {
-  const int nvec = c.d / 8;
-  bwd_dx_kernel<<<(c.T + NW - 1) / NW, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of, dz,
-                                                   static_cast<const uint4*>(Wg), c.T, c.k, c.E,
-                                                   nvec, static_cast<uint4*>(dx));
-  return cudaGetLastError();
+  switch ((c.E + 15) / 16 * 16) {
+    case 16: return launch_dx_ep<16>(c, dxd, slot_of, dz, Wg, dx, s);
+    case 32: return launch_dx_ep<32>(c, dxd, slot_of, dz, Wg, dx, s);
+    case 48: return launch_dx_ep<48>(c, dxd, slot_of, dz, Wg, dx, s);
+    case 64: return launch_dx_ep<64>(c, dxd, slot_of, dz, Wg, dx, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
