@@ -1,8 +1,8 @@
 // Gate-weighted combine and load-balance statistics.
 //
 // Combine: y_t = sum_{j: slot_of[t,j] >= 0} g[t,j] Y[slot_of[t,j]], summed in
-// fp32 in slot order j = 0..k-1 (deterministic: each token is produced by one
-// warp, no atomics); y_t = 0 when every slot of t was dropped. This is the
+// fp32 in slot order j = 0..k-1 (deterministic: each output element is summed
+// by one thread, no atomics); y_t = 0 when every slot of t was dropped. This is the
 // output y = sum_{i in K(x)} g_i(x) E_i(x) of the kwkr.cn MoE article, section
 // 2.1, with the masking of dropped tokens from section 2.3.
 //
@@ -45,6 +45,11 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
 
 // base (optional, [T, d]): each token's sum starts from its base row (the
 // shared expert's output) instead of zero.
+// Warp w of block (bx, by) owns token bx * NW + w and the row chunk by of
+// CHUNK 16-byte vectors (32 lanes x UNR vectors each): a row is split over
+// several warps so that a small batch still fills the GPU, and each lane
+// issues the UNR x k loads of its vectors before it sums them.
+constexpr int UNR = 4, CHUNK = 32 * UNR;
 template <typename T>
 __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y,
                                                      const int32_t* __restrict__ slot_of,
@@ -63,20 +68,38 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y
     sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
     g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
   }
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8];
+  const int v0 = blockIdx.y * CHUNK + lane;
+  float acc[UNR][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    if (base) unpack(__ldg(base + (size_t)t * nvec + v), acc, (T*)nullptr);
+  for (int u = 0; u < UNR; ++u) {
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (sl[j] < 0) continue;
-      float f[8];
-      unpack(__ldg(Y + (size_t)sl[j] * nvec + v), f, (T*)nullptr);
+    for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+    const int v = v0 + 32 * u;
+    if (base && v < nvec) unpack(__ldg(base + (size_t)t * nvec + v), acc[u], (T*)nullptr);
+  }
+  // slot order j = 0..k-1 for every vector: the same fp32 sum order as one
+  // warp walking the row
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], f[i], acc[i]);
+  for (int j = 0; j < kMaxK; ++j) {
+    if (sl[j] < 0) continue;
+    uint4 q[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int v = v0 + 32 * u;
+      q[u] = v < nvec ? __ldg(Y + (size_t)sl[j] * nvec + v) : make_uint4(0, 0, 0, 0);
     }
-    y[(size_t)t * nvec + v] = pack(acc, (T*)nullptr);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      float f[8];
+      unpack(q[u], f, (T*)nullptr);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[u][i] = fmaf(g[j], f[i], acc[u][i]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < UNR; ++u) {
+    const int v = v0 + 32 * u;
+    if (v < nvec) y[(size_t)t * nvec + v] = pack(acc[u], (T*)nullptr);
   }
 }
 
@@ -130,15 +153,15 @@ __global__ void __launch_bounds__(NT) aux_kernel(const int32_t* __restrict__ cou
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
                            const float* gate, void* y, cudaStream_t s, const void* base) {
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
-  const unsigned grid = (unsigned)((c.T + NW - 1) / NW);
+  const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CHUNK - 1) / CHUNK));
   const uint4* b = static_cast<const uint4*>(base);
   const uint4* Yv = static_cast<const uint4*>(Y);
   uint4* yv = static_cast<uint4*>(y);
   if (c.dtype == MOE_F32)
-    return launch_pdl(combine_kernel<float>, dim3(grid), dim3(NT), 0, s, Yv, slot_of, gate, c.T,
-                      c.k, nvec, yv, b);
-  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(NT), 0, s, Yv, slot_of,
-                    gate, c.T, c.k, nvec, yv, b);
+    return launch_pdl(combine_kernel<float>, grid, dim3(NT), 0, s, Yv, slot_of, gate, c.T, c.k,
+                      nvec, yv, b);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(NT), 0, s, Yv, slot_of, gate, c.T,
+                    c.k, nvec, yv, b);
 }
 
 // off[0] = 0, off[1] = rows: the one-group offsets of the shared expert.
