@@ -26,7 +26,8 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/, int H_shared) {
   L.router_tile_hist = take((size_t)router_tc_tiles(c) * E * 4);
   {
     const RouterSplit sp = router_tc_split(c);
-    L.router_split = take(sp.ksplit > 1 ? (size_t)sp.ksplit * T * E * 4 : 4);
+    (void)sp;  // split partials stay in the clusters' shared memory
+    L.router_split = take(4);
   }
   L.disp_hist = take(nblk * E * 4);
   L.disp_base = take((nblk > (size_t)router_tc_tiles(c) ? nblk : (size_t)router_tc_tiles(c)) * E * 4);
@@ -425,12 +426,12 @@ moe_status_t moe_layer_forward_profiled(const moe_config_t* cfg, const moe_layer
 
 int32_t moe_layer_forward_launch_count(const moe_config_t* cfg) {
   if (validate(cfg) != MOE_OK) return 0;
-  // tensor-core router path: router (two kernels when its K range is split),
+  // tensor-core router path: router (one launch; a split K range runs as clusters),
   // dispatch + statistics, gather, GEMM1, GEMM2, and the combine unless k = 1
   // (then GEMM2 writes y). FMA router path: router, dispatch (count, scan,
   // assign, gather), GEMM1, GEMM2, combine, probability reduction, statistics.
   if (router_tc_supported(*cfg))
-    return (cfg->k == 1 ? 5 : 6) + (router_tc_split(*cfg).ksplit > 1 ? 1 : 0);
+    return cfg->k == 1 ? 5 : 6;
   return 10;
 }
 

@@ -14,10 +14,11 @@
 //   warp 0      TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
 //   warp 1      TMEM owner, MMA issuer
 //   warps 2-5   epilogue: one thread per token
-// When the batch has fewer 128-token tiles than the GPU has SMs (e.g. a
-// decode step of 64 tokens), the K range is split over several CTAs per tile
-// (SPLIT): each writes its fp32 partial logits, and router_split_epilogue
-// sums them in a fixed order and runs the same per-token epilogue.
+// When the batch has few 128-token tiles (e.g. a decode step of 64 tokens),
+// the K range of each tile is split over a cluster of CTAs (SPLIT): each
+// leaves its fp32 partial logits in its shared memory, and the cluster's
+// first CTA reads them over distributed shared memory, sums them in split
+// order and runs the same per-token epilogue.
 #include "moe_internal.h"
 #include "tc_ptx.cuh"
 
@@ -391,13 +392,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
       if (SPLIT) {
-        const int t = tile * BM + r;
-        if (t < T) {
-          float* pr = split_part + ((size_t)split * T + t) * E;
+        // this split's partial logits, [EP][128] column-major in the (not yet
+        // used) epilogue scratch, for the cluster's first CTA to read
+        (void)split;
+        float* pt = &st.epi.col[0][0];
 #pragma unroll
-          for (int e = 0; e < EP; ++e)
-            if (e < E) pr[e] = v[e];
-        }
+        for (int e = 0; e < EP; ++e) pt[e * BM + r] = v[e];
       } else {
         router_tile_epilogue<EP>(v, tile, r, etid, bias, noise, tau, T, E, k, logits, idx, gate,
                                  tile_hist, st.epi);
@@ -407,56 +407,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int e = etid; e < E; e += 128) partial[(size_t)blockIdx.x * E + e] = st.epi.part[e];
   }
 
+  if (SPLIT) {
+    // one tile per cluster, split = cluster rank: the first CTA sums the
+    // partials of all ranks in split order (the order of a single pass) and
+    // runs the epilogue; the second cluster barrier keeps every CTA's scratch
+    // alive until it has been read
+    __syncwarp();
+    cluster_sync();
+    if (cluster_ctarank() == 0 && warp >= 2) {
+      const int quarter = warp & 3;
+      const int r = quarter * 32 + lane;
+      const int etid = tid - 64;
+      const int tile = (int)blockIdx.x / ksplit;
+      const float* pt = &st.epi.col[0][0];
+      float v[EP];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) v[e] = 0.f;
+      for (int q = 0; q < ksplit; ++q) {
+        const uint32_t base = cluster_addr(pt, (uint32_t)q) + (uint32_t)r * 4u;
+        float w[EP];
+#pragma unroll
+        for (int e = 0; e < EP; ++e) w[e] = ld_cluster_f32(base + (uint32_t)(e * BM * 4));
+#pragma unroll
+        for (int e = 0; e < EP; ++e) v[e] += w[e];
+      }
+      epi_bar();  // every row is read before the epilogue reuses the scratch
+      router_tile_epilogue<EP>(v, tile, r, etid, bias, noise, tau, T, E, k, logits, idx, gate,
+                               tile_hist, st.epi);
+      for (int e = etid; e < E; e += 128) partial[(size_t)tile * E + e] = st.epi.part[e];
+    }
+    __syncwarp();
+    cluster_sync();
+  }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TCOLS);
-}
-
-// Second pass of the split router: thread r of block `tile` sums the ksplit
-// fp32 partial logits of token tile*128 + r in split order, then runs the
-// per-token epilogue. One block per tile, so the probability partials are
-// per tile.
-template <int EP>
-__global__ void __launch_bounds__(128) router_split_epilogue(
-    const float* __restrict__ split_part, int ksplit, const float* __restrict__ bias,
-    const float* __restrict__ noise, float tau, int T, int E, int k,
-    float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
-    float* __restrict__ partial, int32_t* __restrict__ tile_hist) {
-  __shared__ EpiSmem<EP> es;
-  const int tid = threadIdx.x;
-  const int tile = blockIdx.x;
-  for (int e = tid; e < EP; e += 128) es.part[e] = 0.f;
-  pdl_wait();
-  const int t = tile * BM + tid;
-  float v[EP];
-#pragma unroll
-  for (int e = 0; e < EP; ++e) v[e] = 0.f;
-  if (t < T) {
-    for (int sp = 0; sp < ksplit; ++sp) {
-      const float* pr = split_part + ((size_t)sp * T + t) * E;
-      if ((E & 3) == 0) {  // rows are 16-byte aligned: vector loads
-#pragma unroll
-        for (int e = 0; e < EP; e += 4) {
-          if (e < E) {
-            const float4 q = __ldg(reinterpret_cast<const float4*>(pr + e));
-            v[e] += q.x;
-            v[e + 1] += q.y;
-            v[e + 2] += q.z;
-            v[e + 3] += q.w;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < EP; ++e)
-          if (e < E) v[e] += __ldg(pr + e);
-      }
-    }
-  }
-  __syncthreads();
-  router_tile_epilogue<EP>(v, tile, tid, tid, bias, noise, tau, T, E, k, logits, idx, gate,
-                           tile_hist, es);
-  for (int e = tid; e < E; e += 128) partial[(size_t)tile * E + e] = es.part[e];
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -524,15 +511,12 @@ cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, cons
                       (float*)nullptr);
   }
   if ((e = set_smem_attr<EP, true>()) != cudaSuccess) return e;
-  const int units = router_tc_tiles(c) * sp.ksplit;
-  e = launch_pdl(router_tc_kernel<EP, true>, dim3(units), dim3(NUM_THREADS),
-                 router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau, c.T, c.d, c.E, c.k,
-                 logits, idx, gate, partial, tile_hist, hdr, sp.ksplit, sp.kb_per_split,
-                 split_part);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(router_split_epilogue<EP>, dim3(router_tc_tiles(c)), dim3(128), 0, s,
-                    (const float*)split_part, sp.ksplit, bias, noise, c.tau, c.T, c.E, c.k,
-                    logits, idx, gate, partial, tile_hist);
+  const int units = router_tc_tiles(c) * sp.ksplit;  // one cluster of ksplit CTAs per tile
+  (void)split_part;
+  return launch_pdl_cluster(router_tc_kernel<EP, true>, dim3(units), dim3(NUM_THREADS),
+                            router_smem_bytes<EP>(), sp.ksplit, s, mx, mw, bias, noise, c.tau,
+                            c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr,
+                            sp.ksplit, sp.kb_per_split, (float*)nullptr);
 }
 
 }  // namespace

@@ -181,6 +181,12 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
   return a;
 }
+// A 32-bit load from distributed shared memory (an address from cluster_addr).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // All threads of both CTAs; orders earlier shared-memory writes (mbarrier
 // initialisation included) before the peer's later accesses.
 __device__ __forceinline__ void cluster_sync() {

@@ -130,7 +130,7 @@ def test_launch_count_matches_path():
     from mixture_experts_layer_99_b300 import workloads as W
     L = moe.lib()
     cases = [(W.WORKLOADS["switch_top1"], 5), (W.WORKLOADS["longtail"], 6),
-             (W.WORKLOADS["mixtral"], 6), (W.WORKLOADS["decode"], 7),
+             (W.WORKLOADS["mixtral"], 6), (W.WORKLOADS["decode"], 6),
              (W.WORKLOADS["ref_fp32"], 10), (W.WORKLOADS["sweep_e16_k4"], 6),
              (W.small(W.WORKLOADS["switch_top1"], T=64, d=64, H=64, E=128, k=2), 10)]
     for w, want in cases:
