@@ -107,9 +107,9 @@ inline int router_tc_grid(const moe_config_t& c) {
   return t < kRouterTcMaxBlocks ? t : kRouterTcMaxBlocks;
 }
 // With very few tiles (a batch of at most 16 x 128 tokens) the router splits
-// each tile's K range (64-wide blocks) over up to 8 CTAs; every split is
-// non-empty. Larger batches keep one CTA per tile: measured on B300, the
-// second pass costs more than the split saves once there are 64 tiles.
+// each tile's K range (64-wide blocks) over a cluster of up to 8 CTAs; every
+// split is non-empty. Larger batches keep one CTA per tile: measured on B300,
+// the split's reduction costs more than it saves once there are 64 tiles.
 struct RouterSplit {
   int ksplit, kb_per_split;
 };
