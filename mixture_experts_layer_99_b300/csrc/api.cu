@@ -466,7 +466,8 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
 namespace {
 struct BwdLayout {
   size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W2T, W13T, dz, dg, wg_part,
-      wg_bpart, total;
+      wg_bpart, dzb, WgT, dxr, goff, total;
+  int kp;      // experts padded to a multiple of 64 (K of the dz W_g GEMM)
   int64_t rp;  // padded packed-row bound (columns of the transposed operands)
 };
 BwdLayout bwd_layout(const moe_config_t& c) {
@@ -498,6 +499,11 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.dg = take((size_t)c.T * (size_t)c.k * 4);
   L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
   L.wg_bpart = take((size_t)bwd_wg_splits(c) * E * 4);
+  L.kp = (int)align_up(E, 64);
+  L.dzb = take((size_t)c.T * (size_t)L.kp * 2);
+  L.WgT = take(d * (size_t)L.kp * 2);
+  L.dxr = take((size_t)c.T * d * 2);
+  L.goff = take(8);
   L.total = off;
   return L;
 }
@@ -559,12 +565,22 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   if (e == cudaSuccess && swiglu)
     e = launch_weight_transpose(in->W3, c.E, c.H, c.d, Hp, c.H, W13T, s);
   if (e == cudaSuccess) e = launch_bwd_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s);
+  void* dzb = at<void>(bws, B.dzb);
+  void* WgT = at<void>(bws, B.WgT);
+  void* dxr = at<void>(bws, B.dxr);
+  int32_t* goff = at<int32_t>(bws, B.goff);
   if (e == cudaSuccess)
-    e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz, s);
+    e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz,
+                          dzb, B.kp, s);
+  // router part of dx on the tensor cores: dxr = dz W_g (experts zero-padded)
+  if (e == cudaSuccess) e = cudaMemsetAsync(WgT, 0, (size_t)c.d * B.kp * 2, s);
+  if (e == cudaSuccess) e = launch_weight_transpose(in->Wg, 1, c.E, c.d, B.kp, 0, WgT, s);
+  if (e == cudaSuccess) e = launch_one_group_offsets(goff, c.T, s);
+  if (e == cudaSuccess) e = launch_router_dx_tc(dzb, c.T, B.kp, WgT, c.d, goff, dxr, hdr, s);
   if (e == cudaSuccess)
     e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, W2T, W13T, dYb, pre, dact, dxd, R,
                           hdr, s);
-  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dz, in->Wg, g->dx, s);
+  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s);
   if (e == cudaSuccess)
     e = launch_bwd_wg(c, dz, in->x, at<float>(bws, B.wg_part), at<float>(bws, B.wg_bpart), g->dWg,
                       g->dbias, s);

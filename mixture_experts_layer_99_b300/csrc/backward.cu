@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ gate, const float* __restrict__ dg,
     const float* __restrict__ f, float alpha, float tau, int T, int E, int k,
-    float* __restrict__ dz) {
+    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float p[EP];
@@ -129,61 +129,70 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
   for (int e = 0; e < EP; ++e) pdp = fmaf(p[e], dp[e], pdp);
   const float inv_tau = 1.f / tau;
 #pragma unroll
-  for (int e = 0; e < EP; ++e)
-    if (e < E) dz[(size_t)t * E + e] = p[e] * (dp[e] - pdp) * inv_tau;
+  for (int e = 0; e < EP; ++e) {
+    const float z = e < E ? p[e] * (dp[e] - pdp) * inv_tau : 0.f;
+    if (e < E) dz[(size_t)t * E + e] = z;
+    dp[e] = z;
+  }
+  // bf16 copy with the experts padded to Kp (the operand of the dz W_g GEMM)
+  __nv_bfloat16* zr = dzb + (size_t)t * Kp;
+  for (int e0 = 0; e0 < Kp; e0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < EP; ++q)
+        if (q == e0 + i) v[i] = dp[q];
+    }
+    *reinterpret_cast<uint4*>(zr + e0) = pack8(v);
+  }
 }
 
-// dx_t = sum over the kept slots of dxd[slot] (slot order) + sum_e dz[t, e]
-// Wg[e, :] (a fixed order of the experts), fp32, rounded once. Block = 32 tokens x 256
-// columns: thread c owns one column for the 32 tokens; the block's Wg columns
-// and dz rows are staged in shared memory.
-constexpr int DX_TOK = 32, DX_COLS = 256;
-template <int EP>
-__global__ void __launch_bounds__(DX_COLS) bwd_dx_kernel(const __nv_bfloat16* __restrict__ dxd,
-                                                         const int32_t* __restrict__ slot_of,
-                                                         const float* __restrict__ dz,
-                                                         const __nv_bfloat16* __restrict__ Wg,
-                                                         int T, int k, int E, int d,
-                                                         __nv_bfloat16* __restrict__ dx) {
-  __shared__ __align__(16) float sdz[DX_TOK][EP];
-  __shared__ __nv_bfloat16 swg[EP][DX_COLS];  // <= 32 KB (static shared memory stays < 48 KB)
-  const int c = blockIdx.x * DX_COLS + threadIdx.x;
-  const int t0 = blockIdx.y * DX_TOK;
-  for (int i = threadIdx.x; i < DX_TOK * EP; i += DX_COLS) {
-    const int t = t0 + i / EP, e = i % EP;
-    sdz[i / EP][e] = (t < T && e < E) ? dz[(size_t)t * E + e] : 0.f;
-  }
-#pragma unroll 4
-  for (int e = 0; e < EP; ++e)
-    swg[e][threadIdx.x] = (e < E && c < d) ? Wg[(size_t)e * d + c] : __float2bfloat16_rn(0.f);
-  __syncthreads();
-  if (c >= d) return;
-  float acc[DX_TOK];
+// dx_t = sum over the kept slots of dxd[slot] (slot order) + dxr_t (the
+// router term dz_t W_g from the tensor cores), fp32, rounded once. Warp w of
+// block (bx, by) owns token bx * NW + w and a chunk of 128 16-byte vectors.
+constexpr int DX_UNR = 4, DX_CHUNK = 32 * DX_UNR;
+__global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dxd,
+                                                    const int32_t* __restrict__ slot_of,
+                                                    const uint4* __restrict__ dxr, int T, int k,
+                                                    int nvec, uint4* __restrict__ dx) {
+  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  const int v0 = blockIdx.y * DX_CHUNK + lane;
+  float acc[DX_UNR][8];
 #pragma unroll
-  for (int t = 0; t < DX_TOK; ++t) acc[t] = 0.f;
+  for (int u = 0; u < DX_UNR; ++u)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
   for (int j = 0; j < k; ++j) {
-#pragma unroll 8
-    for (int t = 0; t < DX_TOK; ++t) {
-      if (t0 + t >= T) continue;
-      const int sl = slot_of[(size_t)(t0 + t) * k + j];
-      if (sl >= 0) acc[t] += __bfloat162float(dxd[(size_t)sl * d + c]);
+    const int sl = slot_of[(size_t)t * k + j];
+    if (sl < 0) continue;
+    uint4 q[DX_UNR];
+#pragma unroll
+    for (int u = 0; u < DX_UNR; ++u) {
+      const int v = v0 + 32 * u;
+      q[u] = v < nvec ? __ldg(dxd + (size_t)sl * nvec + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < DX_UNR; ++u) {
+      float a[8];
+      unpack8(q[u], a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
     }
   }
 #pragma unroll
-  for (int e = 0; e < EP; e += 4) {
-    const float w0 = __bfloat162float(swg[e][threadIdx.x]);
-    const float w1 = __bfloat162float(swg[e + 1][threadIdx.x]);
-    const float w2 = __bfloat162float(swg[e + 2][threadIdx.x]);
-    const float w3 = __bfloat162float(swg[e + 3][threadIdx.x]);
+  for (int u = 0; u < DX_UNR; ++u) {
+    const int v = v0 + 32 * u;
+    if (v >= nvec) continue;
+    float a[8];
+    unpack8(__ldg(dxr + (size_t)t * nvec + v), a);
 #pragma unroll
-    for (int t = 0; t < DX_TOK; ++t) {
-      const float4 z = *reinterpret_cast<const float4*>(&sdz[t][e]);
-      acc[t] = fmaf(z.x, w0, fmaf(z.y, w1, fmaf(z.z, w2, fmaf(z.w, w3, acc[t]))));
-    }
+    for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
+    dx[(size_t)t * nvec + v] = pack8(acc[u]);
   }
-#pragma unroll
-  for (int t = 0; t < DX_TOK; ++t)
-    if (t0 + t < T) dx[(size_t)(t0 + t) * d + c] = __float2bfloat16_rn(acc[t]);
 }
 
 // dWg = dz^T x and db = sum_t dz: block (column block cb, token split sp)
@@ -378,9 +387,10 @@ __global__ void __launch_bounds__(128) expert_colsum_kernel(const __nv_bfloat16*
 template <int EP>
 cudaError_t launch_router_bwd_ep(const moe_config_t& c, const float* logits, const int32_t* idx,
                                  const float* gate, const float* dg, const float* f, float alpha,
-                                 float* dz, cudaStream_t s) {
-  bwd_router_kernel<EP><<<(c.T + 127) / 128, 128, 0, s>>>(logits, idx, gate, dg, f, alpha, c.tau,
-                                                          c.T, c.E, c.k, dz);
+                                 float* dz, void* dzb, int Kp, cudaStream_t s) {
+  bwd_router_kernel<EP><<<(c.T + 127) / 128, 128, 0, s>>>(
+      logits, idx, gate, dg, f, alpha, c.tau, c.T, c.E, c.k, dz,
+      static_cast<__nv_bfloat16*>(dzb), Kp);
   return cudaGetLastError();
 }
 
@@ -413,36 +423,25 @@ cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void
 
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, cudaStream_t s) {
+                              float* dz, void* dzb, int Kp, cudaStream_t s) {
   const int ep = (c.E + 15) / 16 * 16;
   switch (ep) {
-    case 16: return launch_router_bwd_ep<16>(c, logits, idx, gate, dg, f, alpha, dz, s);
-    case 32: return launch_router_bwd_ep<32>(c, logits, idx, gate, dg, f, alpha, dz, s);
-    case 48: return launch_router_bwd_ep<48>(c, logits, idx, gate, dg, f, alpha, dz, s);
-    case 64: return launch_router_bwd_ep<64>(c, logits, idx, gate, dg, f, alpha, dz, s);
+    case 16: return launch_router_bwd_ep<16>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+    case 32: return launch_router_bwd_ep<32>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+    case 48: return launch_router_bwd_ep<48>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+    case 64: return launch_router_bwd_ep<64>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
     default: return cudaErrorInvalidValue;
   }
-}
-
-template <int EP>
-cudaError_t launch_dx_ep(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                         const float* dz, const void* Wg, void* dx, cudaStream_t s) {
-  const dim3 grid((unsigned)((c.d + DX_COLS - 1) / DX_COLS), (unsigned)((c.T + DX_TOK - 1) / DX_TOK));
-  bwd_dx_kernel<EP><<<grid, DX_COLS, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(dxd), slot_of, dz, static_cast<const __nv_bfloat16*>(Wg),
-      c.T, c.k, c.E, c.d, static_cast<__nv_bfloat16*>(dx));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const float* dz, const void* Wg, void* dx, cudaStream_t s) {
-  switch ((c.E + 15) / 16 * 16) {
-    case 16: return launch_dx_ep<16>(c, dxd, slot_of, dz, Wg, dx, s);
-    case 32: return launch_dx_ep<32>(c, dxd, slot_of, dz, Wg, dx, s);
-    case 48: return launch_dx_ep<48>(c, dxd, slot_of, dz, Wg, dx, s);
-    case 64: return launch_dx_ep<64>(c, dxd, slot_of, dz, Wg, dx, s);
-    default: return cudaErrorInvalidValue;
-  }
+                          const void* dxr, void* dx, cudaStream_t s) {
+  const int nvec = c.d / 8;
+  const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + DX_CHUNK - 1) / DX_CHUNK));
+  bwd_dx_kernel<<<grid, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of,
+                                    static_cast<const uint4*>(dxr), c.T, c.k, nvec,
+                                    static_cast<uint4*>(dx));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,

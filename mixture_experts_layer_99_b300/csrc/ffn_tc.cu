@@ -873,4 +873,18 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
                                     (int)Hp, nullptr, dxd, rows_bound, hdr, nullptr, nullptr, s);
 }
 
+// Router part of dx in the backward pass: dxr [T, d] = dz [T, Kp] WgT^T with
+// dz in bf16 and the experts zero-padded to Kp (a multiple of 64), WgT [d, Kp]
+// the transposed router weight, one group over all T rows (off = [0, T]).
+cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* WgT, int d,
+                                const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s) {
+  CUtensorMap ma, mb, mo;
+  if (!make_map_2d(&ma, dz_bf16, (uint64_t)Kp, (uint64_t)T) ||
+      !make_map_3d(&mb, WgT, (uint64_t)Kp, (uint64_t)d, 1, UMMA_N) ||
+      !make_map_out(&mo, dxr, (uint64_t)d, (uint64_t)T))
+    return cudaErrorInvalidValue;
+  return launch_gemm<kPlain, false>(false, ma, mb, mb, mo, off, 1, d, Kp, nullptr, dxr, T, hdr,
+                                    nullptr, nullptr, s);
+}
+
 }  // namespace moe

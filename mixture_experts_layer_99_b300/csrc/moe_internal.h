@@ -203,6 +203,8 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
                               const void* W1, const void* W3, const void* b1, const void* W2T,
                               const void* W13T, const void* dY, void* pre, void* dact,
                               void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s);
+cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* WgT, int d,
+                                const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s);
 cudaError_t launch_wgrad_tc(const void* At, const void* Bt, int64_t ld, const int32_t* poff,
                             int E, int M, int N, int m_split, float* out, float* out2,
                             int32_t* hdr, cudaStream_t s);
@@ -212,9 +214,9 @@ cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void
                                cudaStream_t s);
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, cudaStream_t s);
+                              float* dz, void* dz_bf16, int Kp, cudaStream_t s);
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const float* dz, const void* Wg, void* dx, cudaStream_t s);
+                          const void* dxr, void* dx, cudaStream_t s);
 cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
                           float* bpart, float* dWg, float* dbias, cudaStream_t s);
 cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s);
