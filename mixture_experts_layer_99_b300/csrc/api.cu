@@ -466,8 +466,9 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
 namespace {
 struct BwdLayout {
   size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W2T, W13T, dz, dg, wg_part,
-      wg_bpart, dzb, WgT, dxr, goff, total;
+      dzb, WgT, dxr, goff, dzT, xT, wgoff, total;
   int kp;      // experts padded to a multiple of 64 (K of the dz W_g GEMM)
+  int tp;      // tokens padded to a multiple of 64 (K of the dz^T x GEMM)
   int64_t rp;  // padded packed-row bound (columns of the transposed operands)
 };
 BwdLayout bwd_layout(const moe_config_t& c) {
@@ -498,8 +499,11 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.dz = take((size_t)c.T * E * 4);
   L.dg = take((size_t)c.T * (size_t)c.k * 4);
   L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
-  L.wg_bpart = take((size_t)bwd_wg_splits(c) * E * 4);
   L.kp = (int)align_up(E, 64);
+  L.tp = (int)align_up((size_t)c.T, 64);
+  L.dzT = take((size_t)L.kp * (size_t)L.tp * 2);
+  L.xT = take(d * (size_t)L.tp * 2);
+  L.wgoff = take(((size_t)bwd_wg_splits(c) + 1) * 4);
   L.dzb = take((size_t)c.T * (size_t)L.kp * 2);
   L.WgT = take(d * (size_t)L.kp * 2);
   L.dxr = take((size_t)c.T * d * 2);
@@ -569,9 +573,11 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   void* WgT = at<void>(bws, B.WgT);
   void* dxr = at<void>(bws, B.dxr);
   int32_t* goff = at<int32_t>(bws, B.goff);
+  void* dzT = at<void>(bws, B.dzT);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dzT, 0, (size_t)B.kp * B.tp * 2, s);
   if (e == cudaSuccess)
     e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz,
-                          dzb, B.kp, s);
+                          dzb, B.kp, dzT, B.tp, s);
   // router part of dx on the tensor cores: dxr = dz W_g (experts zero-padded)
   if (e == cudaSuccess) e = cudaMemsetAsync(WgT, 0, (size_t)c.d * B.kp * 2, s);
   if (e == cudaSuccess) e = launch_weight_transpose(in->Wg, 1, c.E, c.d, B.kp, 0, WgT, s);
@@ -582,8 +588,9 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
                           hdr, s);
   if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s);
   if (e == cudaSuccess)
-    e = launch_bwd_wg(c, dz, in->x, at<float>(bws, B.wg_part), at<float>(bws, B.wg_bpart), g->dWg,
-                      g->dbias, s);
+    e = launch_bwd_wg(c, dz, dzT, B.kp, in->x, at<void>(bws, B.xT), B.tp,
+                      at<int32_t>(bws, B.wgoff), at<float>(bws, B.wg_part), g->dWg, g->dbias, hdr,
+                      s);
   if (e == cudaSuccess) e = launch_pad_offsets(off, c.E, poff, s);
   if (e == cudaSuccess)
     e = launch_transpose_pad(0, dYb, c.d, c.d, off, poff, c.E, B.rp, at<void>(bws, B.tdY), ldp, s);

@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ gate, const float* __restrict__ dg,
     const float* __restrict__ f, float alpha, float tau, int T, int E, int k,
-    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp) {
+    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp,
+    __nv_bfloat16* __restrict__ dzT, int Tp) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float p[EP];
@@ -134,6 +135,9 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     if (e < E) dz[(size_t)t * E + e] = z;
     dp[e] = z;
   }
+  // transposed bf16 copy [Kp][Tp] (the operand of the dz^T x GEMM)
+#pragma unroll
+  for (int e = 0; e < EP; ++e) dzT[(size_t)e * Tp + t] = __float2bfloat16_rn(dp[e]);
   // bf16 copy with the experts padded to Kp (the operand of the dz W_g GEMM)
   __nv_bfloat16* zr = dzb + (size_t)t * Kp;
   for (int e0 = 0; e0 < Kp; e0 += 8) {
@@ -195,73 +199,38 @@ __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dx
   }
 }
 
-// dWg = dz^T x and db = sum_t dz: block (column block cb, token split sp)
-// writes the partial sums of its tokens; thread c owns column cb*128 + c and
-// all E experts. dz of 32 tokens is staged in shared memory at a time.
-constexpr int WG_COLS = 128, WG_TOK = 32;
-template <int EP>
-__global__ void __launch_bounds__(WG_COLS) bwd_wg_partial_kernel(
-    const float* __restrict__ dz, const __nv_bfloat16* __restrict__ x, int T, int d, int E,
-    int tok_per_split, float* __restrict__ part, float* __restrict__ bpart) {
-  __shared__ __align__(16) float sdz[WG_TOK][EP];
-  __shared__ float sx[WG_TOK][WG_COLS];
-  const int c = blockIdx.x * WG_COLS + threadIdx.x;
-  const int sp = blockIdx.y;
-  const int t0 = sp * tok_per_split;
-  const int t1 = min(T, t0 + tok_per_split);
-  float acc[EP];
-  float bacc = 0.f;
-#pragma unroll
-  for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-  for (int tb = t0; tb < t1; tb += WG_TOK) {
+// db[e] = sum_t dz[t, e]: one block per expert, thread i sums tokens
+// i, i + 256, ... in order, then a fixed-order tree.
+__global__ void __launch_bounds__(256) bwd_dbias_kernel(const float* __restrict__ dz, int T,
+                                                        int E, float* __restrict__ db) {
+  __shared__ float red[256];
+  const int e = blockIdx.x;
+  float s = 0.f;
+  for (int t = threadIdx.x; t < T; t += 256) s += dz[(size_t)t * E + e];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
-    for (int i = threadIdx.x; i < WG_TOK * EP; i += WG_COLS) {
-      const int tt = tb + i / EP, e = i % EP;
-      sdz[i / EP][e] = (tt < t1 && e < E) ? dz[(size_t)tt * E + e] : 0.f;
-    }
-    // this thread's column of the batch's tokens, all loads in flight at once
-#pragma unroll 8
-    for (int i = 0; i < WG_TOK; ++i)
-      sx[i][threadIdx.x] =
-          (tb + i < t1 && c < d) ? __bfloat162float(x[(size_t)(tb + i) * d + c]) : 0.f;
-    __syncthreads();
-#pragma unroll 4
-    for (int i = 0; i < WG_TOK; ++i) {
-      const float xv = sx[i][threadIdx.x];
-#pragma unroll
-      for (int e = 0; e < EP; e += 4) {
-        const float4 z = *reinterpret_cast<const float4*>(&sdz[i][e]);
-        acc[e] = fmaf(z.x, xv, acc[e]);
-        acc[e + 1] = fmaf(z.y, xv, acc[e + 1]);
-        acc[e + 2] = fmaf(z.z, xv, acc[e + 2]);
-        acc[e + 3] = fmaf(z.w, xv, acc[e + 3]);
-      }
-      if (threadIdx.x < EP) bacc += sdz[i][threadIdx.x];
-    }
   }
-  if (c < d) {
-#pragma unroll
-    for (int e = 0; e < EP; ++e)
-      if (e < E) part[((size_t)sp * E + e) * d + c] = acc[e];
-  }
-  if (blockIdx.x == 0 && threadIdx.x < E) bpart[(size_t)sp * E + threadIdx.x] = bacc;
+  if (threadIdx.x == 0) db[e] = red[0];
+}
+
+// Token groups of the dz^T x GEMM: goff[g] = min(g * per, Tp), goff[G] = Tp
+// (a group past the end is empty and its partial is zero).
+__global__ void group_offsets_kernel(int32_t* __restrict__ goff, int G, int per, int Tp) {
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) goff[g] = g < G ? min(g * per, Tp) : Tp;
 }
 
 // Sum of the token-split partials in split order.
-__global__ void bwd_wg_reduce_kernel(const float* __restrict__ part,
-                                     const float* __restrict__ bpart, int nsplit, int E, int d,
-                                     float* __restrict__ dWg, float* __restrict__ dbias) {
+__global__ void bwd_wg_reduce_kernel(const float* __restrict__ part, int nsplit, int E, int d,
+                                     float* __restrict__ dWg) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const int n = E * d;
   if (i < n) {
     float s = 0.f;
     for (int sp = 0; sp < nsplit; ++sp) s += part[(size_t)sp * n + i];
     dWg[i] = s;
-  }
-  if (dbias && i < E) {
-    float s = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) s += bpart[(size_t)sp * E + i];
-    dbias[i] = s;
   }
 }
 
@@ -387,28 +356,28 @@ __global__ void __launch_bounds__(128) expert_colsum_kernel(const __nv_bfloat16*
 template <int EP>
 cudaError_t launch_router_bwd_ep(const moe_config_t& c, const float* logits, const int32_t* idx,
                                  const float* gate, const float* dg, const float* f, float alpha,
-                                 float* dz, void* dzb, int Kp, cudaStream_t s) {
+                                 float* dz, void* dzb, int Kp, void* dzT, int Tp, cudaStream_t s) {
   bwd_router_kernel<EP><<<(c.T + 127) / 128, 128, 0, s>>>(
       logits, idx, gate, dg, f, alpha, c.tau, c.T, c.E, c.k, dz,
-      static_cast<__nv_bfloat16*>(dzb), Kp);
-  return cudaGetLastError();
-}
-
-template <int EP>
-cudaError_t launch_wg_ep(const moe_config_t& c, const float* dz, const void* x, int nsplit,
-                         int tok_per_split, float* part, float* bpart, cudaStream_t s) {
-  const dim3 grid((unsigned)((c.d + WG_COLS - 1) / WG_COLS), (unsigned)nsplit);
-  bwd_wg_partial_kernel<EP><<<grid, WG_COLS, 0, s>>>(
-      dz, static_cast<const __nv_bfloat16*>(x), c.T, c.d, c.E, tok_per_split, part, bpart);
+      static_cast<__nv_bfloat16*>(dzb), Kp, static_cast<__nv_bfloat16*>(dzT), Tp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Token groups of the dz^T x GEMM (each a multiple of 64 tokens, at least
+// 512 when there are enough, at most 64 groups).
 int bwd_wg_splits(const moe_config_t& c) {
-  const int per = 256;  // tokens per split
-  int n = (c.T + per - 1) / per;
-  return n < 1 ? 1 : n;
+  const int tp = (c.T + 63) / 64 * 64;
+  int g = tp / 512;
+  if (g < 1) g = 1;
+  if (g > 64) g = 64;
+  return g;
+}
+int bwd_wg_group_tokens(const moe_config_t& c) {
+  const int tp = (c.T + 63) / 64 * 64;
+  const int g = bwd_wg_splits(c);
+  return ((tp + g - 1) / g + 63) / 64 * 64;
 }
 
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
@@ -423,15 +392,18 @@ cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void
 
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, void* dzb, int Kp, cudaStream_t s) {
+                              float* dz, void* dzb, int Kp, void* dzT, int Tp, cudaStream_t s) {
   const int ep = (c.E + 15) / 16 * 16;
+#define MOE_RB(EPV) \
+  launch_router_bwd_ep<EPV>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, dzT, Tp, s)
   switch (ep) {
-    case 16: return launch_router_bwd_ep<16>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
-    case 32: return launch_router_bwd_ep<32>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
-    case 48: return launch_router_bwd_ep<48>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
-    case 64: return launch_router_bwd_ep<64>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+    case 16: return MOE_RB(16);
+    case 32: return MOE_RB(32);
+    case 48: return MOE_RB(48);
+    case 64: return MOE_RB(64);
     default: return cudaErrorInvalidValue;
   }
+#undef MOE_RB
 }
 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
@@ -444,23 +416,32 @@ cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t*
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
-                          float* bpart, float* dWg, float* dbias, cudaStream_t s) {
-  const int nsplit = bwd_wg_splits(c);
-  const int per = (c.T + nsplit - 1) / nsplit;
-  const int ep = (c.E + 15) / 16 * 16;
-  cudaError_t e;
-  switch (ep) {
-    case 16: e = launch_wg_ep<16>(c, dz, x, nsplit, per, part, bpart, s); break;
-    case 32: e = launch_wg_ep<32>(c, dz, x, nsplit, per, part, bpart, s); break;
-    case 48: e = launch_wg_ep<48>(c, dz, x, nsplit, per, part, bpart, s); break;
-    case 64: e = launch_wg_ep<64>(c, dz, x, nsplit, per, part, bpart, s); break;
-    default: return cudaErrorInvalidValue;
-  }
+// dWg = dz^T x on the tensor cores: token groups of the weight-gradient GEMM
+// (At = dz^T [Kp][Tp], Bt = x^T [d][Tp]) give fp32 partials [G][E][d], summed
+// in group order; db = column sums of dz.
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzT, int Kp,
+                          const void* x, void* xT, int Tp, int32_t* goff, float* part,
+                          float* dWg, float* dbias, int32_t* hdr, cudaStream_t s) {
+  const int G = bwd_wg_splits(c), per = bwd_wg_group_tokens(c);
+  (void)Kp;
+  const int t8 = (c.T + 7) / 8 * 8;
+  cudaError_t e = launch_weight_transpose(x, 1, c.T, c.d, Tp, 0, xT, s);
+  if (e == cudaSuccess && Tp > t8)
+    e = cudaMemset2DAsync(static_cast<__nv_bfloat16*>(xT) + t8, (size_t)Tp * 2, 0,
+                          (size_t)(Tp - t8) * 2, (size_t)c.d, s);
+  if (e != cudaSuccess) return e;
+  group_offsets_kernel<<<1, 128, 0, s>>>(goff, G, per, Tp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_wgrad_tc(dzT, xT, Tp, goff, G, c.E, c.d, c.E, part, part, hdr, s);
   if (e != cudaSuccess) return e;
   const int n = c.E * c.d;
-  bwd_wg_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, bpart, nsplit, c.E, c.d, dWg, dbias);
-  return cudaGetLastError();
+  bwd_wg_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, G, c.E, c.d, dWg);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (dbias) {
+    bwd_dbias_kernel<<<c.E, 256, 0, s>>>(dz, c.T, c.E, dbias);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s) {

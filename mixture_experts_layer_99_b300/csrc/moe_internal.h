@@ -214,11 +214,14 @@ cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void
                                cudaStream_t s);
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, void* dz_bf16, int Kp, cudaStream_t s);
+                              float* dz, void* dz_bf16, int Kp, void* dzT, int Tp,
+                              cudaStream_t s);
+int bwd_wg_group_tokens(const moe_config_t& c);
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
                           const void* dxr, void* dx, cudaStream_t s);
-cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* x, float* part,
-                          float* bpart, float* dWg, float* dbias, cudaStream_t s);
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzT, int Kp,
+                          const void* x, void* xT, int Tp, int32_t* goff, float* part,
+                          float* dWg, float* dbias, int32_t* hdr, cudaStream_t s);
 cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s);
 cudaError_t launch_transpose_pad(int act, const void* in, int ld_in, int C, const int32_t* off,
                                  const int32_t* poff, int E, int64_t rp_bound, void* out,
