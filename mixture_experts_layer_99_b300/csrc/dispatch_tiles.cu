@@ -69,10 +69,20 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     if (tid < G * E) {
       const int e = tid % E, g = tid / E;
       int st = 0, sb = 0;
-      for (int tt = g; tt < ntiles; tt += G) {
-        const int v = tile_hist[(size_t)tt * E + e];
-        st += v;
-        if (tt < tile) sb += v;
+      // eight independent loads in flight per round (at E = 64 a thread
+      // reads every 4th of 256 tiles)
+      for (int tt0 = g; tt0 < ntiles; tt0 += 8 * G) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int tt = tt0 + i * G;
+          v[i] = tt < ntiles ? tile_hist[(size_t)tt * E + e] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          st += v[i];
+          if (tt0 + i * G < tile) sb += v[i];
+        }
       }
       ptot[g * E + e] = st;
       pbase[g * E + e] = sb;
