@@ -10,10 +10,14 @@
 //
 // The contraction x Wg^T (E tiny) is HBM-bound: the kernel streams 128-token
 // tiles of x through TMA and issues one 128 x E_pad x 16 MMA per 16-wide K
-// step, so each epilogue thread owns one token's whole logit row in TMEM.
-//   warp 0      TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
-//   warp 1      TMEM owner, MMA issuer
-//   warps 2-5   epilogue: one thread per token
+// step into a TMEM accumulator row per token.
+//   warp 0       TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
+//   warp 1       TMEM owner, MMA issuer
+//   warps 2-17   epilogue, four threads per token: warps 2-5 move the
+//                tile's logits from TMEM to shared memory (one row per
+//                token), then each token's four threads take a quarter of
+//                its experts each and combine max, top-k and the softmax sum
+//                with shuffles
 // When the batch has few 128-token tiles (e.g. a decode step of 64 tokens),
 // the K range of each tile is split over a cluster of CTAs (SPLIT): each
 // leaves its fp32 partial logits in its shared memory, and the cluster's
@@ -32,15 +36,19 @@ using namespace ptx;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NUM_THREADS = 192;
+constexpr int TPT = 4;                         // epilogue threads per token
+constexpr int EPI_THREADS = BM * TPT;          // 512
+constexpr int NUM_THREADS = 64 + EPI_THREADS;  // + producer and MMA warps
 constexpr int A_BYTES = BM * BK * 2;
 
-// Epilogue scratch: the tile's probabilities, one padded row per token (an odd
-// row stride keeps both the row writes and the column reads conflict-free),
-// summed per expert down the columns.
+// Epilogue scratch: the tile's logits, then its probabilities, one row per
+// token padded by four floats (16-byte rows whose banks shift by 4 or 20 from
+// row to row, so the 16-byte row accesses are conflict-free), summed per
+// expert down the columns.
+constexpr int LPAD = 4;
 template <int EP>
 struct EpiSmem {
-  float col[BM][EP + 1];
+  alignas(16) float L[BM][EP + LPAD];
   float part[EP];
   int hist[EP];
 };
@@ -49,9 +57,9 @@ template <int EP>
 struct RouterCfg {
   static constexpr int B_BYTES = EP * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  // as many operand stages (at most 8) as fit beside the epilogue scratch
+  // as many operand stages (at most 12) as fit beside the epilogue scratch
   static constexpr int FIT = (int)((220 * 1024 - sizeof(EpiSmem<EP>) - 1024 - 256) / STAGE);
-  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int STAGES = FIT > 12 ? 12 : FIT;
   static constexpr int TCOLS = 2 * EP <= 32 ? 32 : (2 * EP <= 64 ? 64 : 128);
 };
 
@@ -72,8 +80,22 @@ constexpr size_t router_smem_bytes() {
   return 1024 + RouterCfg<EP>::STAGES * RouterCfg<EP>::STAGE + sizeof(RouterSmem<EP>);
 }
 
-__device__ __forceinline__ void epi_bar() {  // named barrier over the 4 epilogue warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+__device__ __forceinline__ void epi_bar() {  // named barrier over the 16 epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+}
+// The same barrier, returning whether any epilogue thread passed `fail`: one
+// decision that every epilogue thread takes alike.
+__device__ __forceinline__ bool epi_bar_or(bool fail) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)fail), "n"(EPI_THREADS)
+      : "memory");
+  return r != 0;
 }
 
 template <int EP>
@@ -97,145 +119,212 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[EP]) {
   }
 }
 
-// One token per thread (thread r of the 128 owns token tile*128 + r): keys,
-// softmax, top-k (descending, ties to the lower index), gates, and the
-// tile's per-expert selection counts and sums of p (fixed order).
+// Thread p's quarter of token r's row of the scratch (Q = EP/4 floats, a
+// multiple of 4).
 template <int EP>
+__device__ __forceinline__ void load_quarter(const EpiSmem<EP>& es, int r, int p,
+                                             float (&v)[EP / TPT]) {
+  constexpr int Q = EP / TPT;
+  const float4* row = reinterpret_cast<const float4*>(&es.L[r][p * Q]);
+#pragma unroll
+  for (int q = 0; q < Q; q += 4) {
+    const float4 w = row[q / 4];
+    v[q] = w.x;
+    v[q + 1] = w.y;
+    v[q + 2] = w.z;
+    v[q + 3] = w.w;
+  }
+}
+
+// (value, expert) a ranks before b: larger value, ties to the lower index.
+__device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// One token's four threads (lanes 4j..4j+3 of a warp; thread p owns experts
+// [p Q, p Q + Q), Q = EP/4): keys, softmax, top-k (descending, ties to the
+// lower index), gates, and the tile's per-expert selection counts and sums of
+// p (fixed order). v holds the thread's Q raw logits on entry.
+template <int EP, int KM>
 __device__ __forceinline__ void router_tile_epilogue(
-    float (&v)[EP], int tile, int r, int etid, const float* __restrict__ bias,
+    float (&v)[EP / TPT], int tile, int r, int p, int etid, const float* __restrict__ bias,
     const float* __restrict__ noise, float tau, int T, int E, int k, float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ gate, int32_t* __restrict__ tile_hist,
     EpiSmem<EP>& es) {
-  for (int e = etid; e < EP; e += 128) es.hist[e] = 0;
+  constexpr int Q = EP / TPT;
   const int t = tile * BM + r;
   const bool valid = t < T;
+  const int e0 = p * Q;
   const bool vec4 = (E & 3) == 0;  // rows of [T, E] fp32 arrays are 16-byte aligned
   // selection keys l = (z + b + g) / tau (one reciprocal; tau = 1 leaves them as they are)
   if (valid) {
     if (bias) {
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) v[e] += __ldg(bias + e);
+      for (int q = 0; q < Q; ++q)
+        if (e0 + q < E) v[q] += __ldg(bias + e0 + q);
     }
     if (noise) {
-      const float* nr = noise + (size_t)t * E;
+      const float* nr = noise + (size_t)t * E + e0;
       if (vec4) {
 #pragma unroll
-        for (int e = 0; e < EP; e += 4) {
-          if (e < E) {
-            const float4 q = __ldg(reinterpret_cast<const float4*>(nr + e));
-            v[e] += q.x;
-            v[e + 1] += q.y;
-            v[e + 2] += q.z;
-            v[e + 3] += q.w;
+        for (int q = 0; q < Q; q += 4) {
+          if (e0 + q < E) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(nr + q));
+            v[q] += w.x;
+            v[q + 1] += w.y;
+            v[q + 2] += w.z;
+            v[q + 3] += w.w;
           }
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < EP; ++e)
-          if (e < E) v[e] += __ldg(nr + e);
+        for (int q = 0; q < Q; ++q)
+          if (e0 + q < E) v[q] += __ldg(nr + q);
       }
     }
     if (tau != 1.f) {
       const float inv_tau = 1.f / tau;
 #pragma unroll
-      for (int e = 0; e < EP; ++e) v[e] *= inv_tau;
+      for (int q = 0; q < Q; ++q) v[q] *= inv_tau;
     }
   }
 #pragma unroll
-  for (int e = 0; e < EP; ++e)
-    if (e >= E) v[e] = -INFINITY;
+  for (int q = 0; q < Q; ++q)
+    if (e0 + q >= E) v[q] = -INFINITY;
   float m = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < EP; ++e) m = fmaxf(m, v[e]);
+  for (int q = 0; q < Q; ++q) m = fmaxf(m, v[q]);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   if (valid && logits) {
-    float* lr = logits + (size_t)t * E;
+    float* lr = logits + (size_t)t * E + e0;
     if (vec4) {
 #pragma unroll
-      for (int e = 0; e < EP; e += 4)
-        if (e < E) *reinterpret_cast<float4*>(lr + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      for (int q = 0; q < Q; q += 4)
+        if (e0 + q < E) *reinterpret_cast<float4*>(lr + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     } else {
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) lr[e] = v[e];
+      for (int q = 0; q < Q; ++q)
+        if (e0 + q < E) lr[q] = v[q];
     }
   }
-  // top-k on the keys: descending, ties to the lower index
-  uint64_t taken = 0;
-  float selv[kMaxK];
-  int seli[kMaxK];
+  // top-KM of this thread's experts, best first; (-inf, INT_MAX) ranks last
+  float sv[KM];
+  int si[KM];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    selv[j] = -INFINITY;
-    seli[j] = 0;
-    if (j < k) {
-      float bv = -INFINITY;
-      int bi = -1;
+  for (int j = 0; j < KM; ++j) {
+    sv[j] = -INFINITY;
+    si[j] = 0x7fffffff;
+  }
 #pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        const bool free_ = e < E && !((taken >> e) & 1ull);
-        if (free_ && (bi < 0 || v[e] > bv)) {
-          bv = v[e];
-          bi = e;
+  for (int q = 0; q < Q; ++q) {
+    float cv = v[q];
+    int ci = e0 + q;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (ranks_before(cv, ci, sv[j], si[j])) {
+        const float tv = sv[j];
+        const int ti = si[j];
+        sv[j] = cv;
+        si[j] = ci;
+        cv = tv;
+        ci = ti;
+      }
+    }
+  }
+  // merge with the other three threads' lists: the pairwise better of a[j]
+  // and b[KM-1-j] are the top KM of both (a bitonic sequence), then sorted
+  // by half-cleaners; all four threads end with the same list
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    float ov[KM];
+    int oi[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      ov[j] = __shfl_xor_sync(0xffffffffu, sv[j], o);
+      oi[j] = __shfl_xor_sync(0xffffffffu, si[j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (ranks_before(ov[KM - 1 - j], oi[KM - 1 - j], sv[j], si[j])) {
+        sv[j] = ov[KM - 1 - j];
+        si[j] = oi[KM - 1 - j];
+      }
+    }
+#pragma unroll
+    for (int h = KM / 2; h >= 1; h >>= 1) {
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        if ((j & h) == 0 && ranks_before(sv[j + h], si[j + h], sv[j], si[j])) {
+          const float tv = sv[j];
+          const int ti = si[j];
+          sv[j] = sv[j + h];
+          si[j] = si[j + h];
+          sv[j + h] = tv;
+          si[j + h] = ti;
         }
       }
-      if (bi < 0) bi = 0;
-      taken |= 1ull << bi;
-      selv[j] = bv;
-      seli[j] = bi;
     }
   }
-  __syncwarp();
-  epi_bar();  // hist zeroed; the previous tile's column sums are done
-  if (valid) {
+  // probabilities for the statistics P_i, back into the token's row
+  {
+    float sum = 0.f;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      v[q] = (e0 + q < E && valid) ? __expf(v[q] - m) : 0.f;
+      sum += v[q];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    const float inv_s = valid ? 1.f / sum : 0.f;
+    float4* row = reinterpret_cast<float4*>(&es.L[r][e0]);
+#pragma unroll
+    for (int q = 0; q < Q; q += 4)
+      row[q / 4] = make_float4(v[q] * inv_s, v[q + 1] * inv_s, v[q + 2] * inv_s, v[q + 3] * inv_s);
+  }
+  if (valid && p == 0) {
     // gates from the selected keys only: g_j = p_j / sum_m p_m, where the
     // softmax denominator cancels
-    float psel[kMaxK], psum = 0.f;
+    float psel[KM], psum = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (j < k) {
-        psel[j] = expf(selv[j] - m);
+        psel[j] = expf(sv[j] - m);
         psum += psel[j];
       }
     }
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KM; ++j) {
       if (j < k) {
-        idx[(size_t)t * k + j] = seli[j];
+        const int ej = si[j] < E ? si[j] : 0;
+        idx[(size_t)t * k + j] = ej;
         gate[(size_t)t * k + j] = psel[j] / psum;
-        atomicAdd(&es.hist[seli[j]], 1);
+        atomicAdd(&es.hist[ej], 1);
       }
     }
   }
-  // probabilities for the statistics P_i: one row per token in shared memory
+  epi_bar();  // probabilities and counts of the whole tile are in place
+  // per-expert sums over the tile's 128 tokens: eight threads per expert each
+  // walk 16 rows in token order, then a fixed butterfly adds the eight
   {
-    float s = 0.f;
+    const int e = etid >> 3, q8 = etid & 7;
+    float a = 0.f;
+    if (e < E) {
 #pragma unroll
-    for (int e = 0; e < EP; ++e) {
-      v[e] = (e < E && valid) ? __expf(v[e] - m) : 0.f;
-      s += v[e];
+      for (int i = 0; i < 16; ++i) a += es.L[16 * q8 + i][e];
     }
-    const float inv_s = valid ? 1.f / s : 0.f;
-#pragma unroll
-    for (int e = 0; e < EP; ++e) es.col[r][e] = v[e] * inv_s;
-  }
-  epi_bar();
-  // per-expert sums over the tile's 128 tokens: one thread per expert walks
-  // its column in token order (two interleaved partial sums, then added)
-  for (int e = etid; e < E; e += 128) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-    for (int rr = 0; rr < BM; rr += 2) {
-      a0 += es.col[rr][e];
-      a1 += es.col[rr + 1][e];
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    a += __shfl_xor_sync(0xffffffffu, a, 4);
+    if (q8 == 0 && e < E) {
+      es.part[e] += a;
+      if (tile_hist) tile_hist[(size_t)tile * E + e] = es.hist[e];
     }
-    es.part[e] += a0 + a1;
-    if (tile_hist) tile_hist[(size_t)tile * E + e] = es.hist[e];
   }
-  epi_bar();
+  epi_bar();  // the scratch and the counts are free for the next tile
 }
 
-template <int EP, bool SPLIT>
+template <int EP, int KM, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const float* __restrict__ bias,
@@ -373,71 +462,104 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue: thread r of the tile owns token tile*128 + r
+    // ---------------- epilogue: warps 2-5 read TMEM (thread = token row);
+    // epilogue thread etid works on token etid / 4, experts quarter etid % 4
+    constexpr int Q = EP / TPT;
+    const int etid = tid - 64;  // 0..511
+    const bool tmem_warp = warp < 6;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int etid = tid - 64;  // 0..127
+    const int lr = quarter * 32 + lane;  // the TMEM lane (token row) a TMEM warp reads
+    const int r = etid >> 2, p = etid & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-      const int tile = u / ksplit, split = u % ksplit;
-      if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) break;
-      tc_fence_after();
-      float v[EP];
-      tmem_ld_row<EP>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * EP), v);
-      tc_fence_before();
-      mbar_arrive(&st.tmem_empty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-      if (SPLIT) {
-        // this split's partial logits, [EP][128] column-major in the (not yet
-        // used) epilogue scratch, for the cluster's first CTA to read
-        (void)split;
-        float* pt = &st.epi.col[0][0];
+      const int tile = u / ksplit;
+      bool fail = false;
+      if (tmem_warp) {
+        if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) {
+          fail = true;
+        } else {
+          tc_fence_after();
+          float v[EP];
+          tmem_ld_row<EP>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * EP), v);
+          tc_fence_before();
+          mbar_arrive(&st.tmem_empty[acc]);
+          // the token's (partial) logits, one row of the scratch
+          float4* row = reinterpret_cast<float4*>(&st.epi.L[lr][0]);
 #pragma unroll
-        for (int e = 0; e < EP; ++e) pt[e * BM + r] = v[e];
-      } else {
-        router_tile_epilogue<EP>(v, tile, r, etid, bias, noise, tau, T, E, k, logits, idx, gate,
-                                 tile_hist, st.epi);
+          for (int e = 0; e < EP; e += 4) row[e / 4] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (etid < EP) st.epi.hist[etid] = 0;
+      if (epi_bar_or(fail)) break;  // the tile's logits are in shared memory
+      if (!SPLIT) {
+        float v[Q];
+        load_quarter<EP>(st.epi, r, p, v);
+        router_tile_epilogue<EP, KM>(v, tile, r, p, etid, bias, noise, tau, T, E, k, logits, idx,
+                                     gate, tile_hist, st.epi);
       }
     }
     if (!SPLIT)
-      for (int e = etid; e < E; e += 128) partial[(size_t)blockIdx.x * E + e] = st.epi.part[e];
+      for (int e = etid; e < E; e += EPI_THREADS) partial[(size_t)blockIdx.x * E + e] = st.epi.part[e];
   }
 
   if (SPLIT) {
-    // one tile per cluster, split = cluster rank: the first CTA sums the
-    // partials of all ranks in split order (the order of a single pass) and
-    // runs the epilogue; the second cluster barrier keeps every CTA's scratch
-    // alive until it has been read
+    // one tile per cluster, split = cluster rank. Every rank sums one slice
+    // of the columns (CW experts, 16-byte pieces) over all ranks' partial
+    // logits in split order (the order of a single pass) and writes the sums
+    // into the first CTA's scratch, which then runs the epilogue. The cluster
+    // barriers order: partials written / slices read / sums written.
+    static_assert(EP % 4 == 0 && BM * (EP / 2 / 4) <= 2 * EPI_THREADS, "two pieces per thread");
+    const uint32_t my = cluster_ctarank();
+    const int CW = ((EP + ksplit - 1) / ksplit + 3) / 4 * 4;
+    const int c0 = (int)my * CW;
+    const int nv = c0 < EP ? (min(EP, c0 + CW) - c0) / 4 : 0;  // pieces per row
+    const int etid = tid - 64;
+    float4 acc4[2];
+    int row4[2], col4[2];
     __syncwarp();
     cluster_sync();
-    if (cluster_ctarank() == 0 && warp >= 2) {
-      const int quarter = warp & 3;
-      const int r = quarter * 32 + lane;
-      const int etid = tid - 64;
-      const int tile = (int)blockIdx.x / ksplit;
-      const float* pt = &st.epi.col[0][0];
-      float v[EP];
 #pragma unroll
-      for (int e = 0; e < EP; ++e) v[e] = 0.f;
-      for (int q = 0; q < ksplit; ++q) {
-        const uint32_t base = cluster_addr(pt, (uint32_t)q) + (uint32_t)r * 4u;
-        float w[EP];
-#pragma unroll
-        for (int e = 0; e < EP; ++e) w[e] = ld_cluster_f32(base + (uint32_t)(e * BM * 4));
-#pragma unroll
-        for (int e = 0; e < EP; ++e) v[e] += w[e];
+    for (int it = 0; it < 2; ++it) {
+      acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int item = etid + it * EPI_THREADS;
+      row4[it] = -1;
+      col4[it] = 0;
+      if (warp >= 2 && item < BM * nv) {
+        row4[it] = item / nv;
+        col4[it] = c0 + 4 * (item % nv);
+        for (int qq = 0; qq < ksplit; ++qq) {
+          const float4 w = ld_cluster_v4(cluster_addr(&st.epi.L[row4[it]][col4[it]], (uint32_t)qq));
+          acc4[it].x += w.x;
+          acc4[it].y += w.y;
+          acc4[it].z += w.z;
+          acc4[it].w += w.w;
+        }
       }
-      epi_bar();  // every row is read before the epilogue reuses the scratch
-      router_tile_epilogue<EP>(v, tile, r, etid, bias, noise, tau, T, E, k, logits, idx, gate,
-                               tile_hist, st.epi);
-      for (int e = etid; e < E; e += 128) partial[(size_t)tile * E + e] = st.epi.part[e];
     }
     __syncwarp();
-    cluster_sync();
+    cluster_sync();  // every slice is read before the first CTA's scratch is overwritten
+#pragma unroll
+    for (int it = 0; it < 2; ++it)
+      if (row4[it] >= 0) st_cluster_v4(cluster_addr(&st.epi.L[row4[it]][col4[it]], 0u), acc4[it]);
+    __syncwarp();
+    cluster_sync();  // the summed logits are in the first CTA's scratch
+    if (my == 0 && warp >= 2) {
+      constexpr int Q = EP / TPT;
+      const int r = etid >> 2, p = etid & 3;
+      const int tile = (int)blockIdx.x / ksplit;
+      float v[Q];
+      load_quarter<EP>(st.epi, r, p, v);
+      if (etid < EP) st.epi.hist[etid] = 0;
+      epi_bar();  // counts zeroed before the epilogue's atomics
+      router_tile_epilogue<EP, KM>(v, tile, r, p, etid, bias, noise, tau, T, E, k, logits, idx,
+                                   gate, tile_hist, st.epi);
+      for (int e = etid; e < E; e += EPI_THREADS) partial[(size_t)tile * E + e] = st.epi.part[e];
+    }
   }
 
   tc_fence_before();
@@ -477,14 +599,14 @@ bool map_rows(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EP, bool SPLIT>
+template <int EP, int KM, bool SPLIT>
 cudaError_t set_smem_attr() {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(router_tc_kernel<EP, SPLIT>,
+    e = cudaFuncSetAttribute(router_tc_kernel<EP, KM, SPLIT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)router_smem_bytes<EP>());
     if (e != cudaSuccess) return e;
@@ -493,6 +615,30 @@ cudaError_t set_smem_attr() {
   return cudaSuccess;
 }
 
+template <int EP, int KM>
+cudaError_t launch_ep_km(const moe_config_t& c, const CUtensorMap& mx, const CUtensorMap& mw,
+                         const float* bias, const float* noise, float* logits, int32_t* idx,
+                         float* gate, float* partial, int32_t* tile_hist, int32_t* hdr,
+                         cudaStream_t s) {
+  static_assert(router_smem_bytes<EP>() <= 227 * 1024, "router shared memory over the per-CTA limit");
+  const RouterSplit sp = router_tc_split(c);
+  cudaError_t e;
+  if (sp.ksplit == 1) {
+    if ((e = set_smem_attr<EP, KM, false>()) != cudaSuccess) return e;
+    return launch_pdl(router_tc_kernel<EP, KM, false>, dim3(router_tc_grid(c)),
+                      dim3(NUM_THREADS), router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau,
+                      c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr, 1,
+                      sp.kb_per_split, (float*)nullptr);
+  }
+  if ((e = set_smem_attr<EP, KM, true>()) != cudaSuccess) return e;
+  const int units = router_tc_tiles(c) * sp.ksplit;  // one cluster of ksplit CTAs per tile
+  return launch_pdl_cluster(router_tc_kernel<EP, KM, true>, dim3(units), dim3(NUM_THREADS),
+                            router_smem_bytes<EP>(), sp.ksplit, s, mx, mw, bias, noise, c.tau,
+                            c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr,
+                            sp.ksplit, sp.kb_per_split, (float*)nullptr);
+}
+
+// k <= 2 sorts candidate lists of two entries, larger k lists of eight.
 template <int EP>
 cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
                       const float* noise, float* logits, int32_t* idx, float* gate,
@@ -501,22 +647,12 @@ cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, cons
   CUtensorMap mx, mw;
   if (!map_rows(&mx, x, c.d, c.T, BM) || !map_rows(&mw, Wg, c.d, c.E, EP))
     return cudaErrorInvalidValue;
-  const RouterSplit sp = router_tc_split(c);
-  cudaError_t e;
-  if (sp.ksplit == 1) {
-    if ((e = set_smem_attr<EP, false>()) != cudaSuccess) return e;
-    return launch_pdl(router_tc_kernel<EP, false>, dim3(router_tc_grid(c)), dim3(NUM_THREADS),
-                      router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau, c.T, c.d, c.E,
-                      c.k, logits, idx, gate, partial, tile_hist, hdr, 1, sp.kb_per_split,
-                      (float*)nullptr);
-  }
-  if ((e = set_smem_attr<EP, true>()) != cudaSuccess) return e;
-  const int units = router_tc_tiles(c) * sp.ksplit;  // one cluster of ksplit CTAs per tile
   (void)split_part;
-  return launch_pdl_cluster(router_tc_kernel<EP, true>, dim3(units), dim3(NUM_THREADS),
-                            router_smem_bytes<EP>(), sp.ksplit, s, mx, mw, bias, noise, c.tau,
-                            c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr,
-                            sp.ksplit, sp.kb_per_split, (float*)nullptr);
+  if (c.k <= 2)
+    return launch_ep_km<EP, 2>(c, mx, mw, bias, noise, logits, idx, gate, partial, tile_hist,
+                               hdr, s);
+  return launch_ep_km<EP, kMaxK>(c, mx, mw, bias, noise, logits, idx, gate, partial, tile_hist,
+                                 hdr, s);
 }
 
 }  // namespace
