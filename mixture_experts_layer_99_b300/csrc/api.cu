@@ -465,8 +465,8 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {
-  size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W2T, W13T, dz, dg, wg_part,
-      dzb, WgT, dxr, goff, dzT, xT, wgoff, total;
+  size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W13T, dz, dg, wg_part, dzb, dxr,
+      goff, dzT, xT, wgoff, total;
   int kp;      // experts padded to a multiple of 64 (K of the dz W_g GEMM)
   int tp;      // tokens padded to a multiple of 64 (K of the dz^T x GEMM)
   int64_t rp;  // padded packed-row bound (columns of the transposed operands)
@@ -494,8 +494,7 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.th = take(H * rp * 2);
   L.tdact = take(Hp * rp * 2);
   L.txd = take(d * rp * 2);
-  L.W2T = take(E * H * d * 2);
-  L.W13T = take(E * d * Hp * 2);
+  L.W13T = take(bwd_w13_transposed(c) ? E * d * Hp * 2 : 0);
   L.dz = take((size_t)c.T * E * 4);
   L.dg = take((size_t)c.T * (size_t)c.k * 4);
   L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
@@ -505,7 +504,6 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.xT = take(d * (size_t)L.tp * 2);
   L.wgoff = take(((size_t)bwd_wg_splits(c) + 1) * 4);
   L.dzb = take((size_t)c.T * (size_t)L.kp * 2);
-  L.WgT = take(d * (size_t)L.kp * 2);
   L.dxr = take((size_t)c.T * d * 2);
   L.goff = take(8);
   L.total = off;
@@ -559,18 +557,17 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   void* dYb = at<void>(bws, B.dY);
   void* dxd = at<void>(bws, B.dxd);
   int32_t* poff = at<int32_t>(bws, B.poff);
-  void* W2T = at<void>(bws, B.W2T);
-  void* W13T = at<void>(bws, B.W13T);
+  void* W13T = bwd_w13_transposed(c) ? at<void>(bws, B.W13T) : nullptr;
   float* dz = at<float>(bws, B.dz);
   float* dg = at<float>(bws, B.dg);
   const int ldp = (int)B.rp;
-  cudaError_t e = launch_weight_transpose(in->W2, c.E, c.d, c.H, c.d, 0, W2T, s);
-  if (e == cudaSuccess) e = launch_weight_transpose(in->W1, c.E, c.H, c.d, Hp, 0, W13T, s);
-  if (e == cudaSuccess && swiglu)
-    e = launch_weight_transpose(in->W3, c.E, c.H, c.d, Hp, c.H, W13T, s);
+  cudaError_t e = cudaSuccess;
+  if (W13T) {
+    e = launch_weight_transpose(in->W1, c.E, c.H, c.d, Hp, 0, W13T, s);
+    if (e == cudaSuccess) e = launch_weight_transpose(in->W3, c.E, c.H, c.d, Hp, c.H, W13T, s);
+  }
   if (e == cudaSuccess) e = launch_bwd_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s);
   void* dzb = at<void>(bws, B.dzb);
-  void* WgT = at<void>(bws, B.WgT);
   void* dxr = at<void>(bws, B.dxr);
   int32_t* goff = at<int32_t>(bws, B.goff);
   void* dzT = at<void>(bws, B.dzT);
@@ -579,13 +576,12 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
     e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz,
                           dzb, B.kp, dzT, B.tp, s);
   // router part of dx on the tensor cores: dxr = dz W_g (experts zero-padded)
-  if (e == cudaSuccess) e = cudaMemsetAsync(WgT, 0, (size_t)c.d * B.kp * 2, s);
-  if (e == cudaSuccess) e = launch_weight_transpose(in->Wg, 1, c.E, c.d, B.kp, 0, WgT, s);
   if (e == cudaSuccess) e = launch_one_group_offsets(goff, c.T, s);
-  if (e == cudaSuccess) e = launch_router_dx_tc(dzb, c.T, B.kp, WgT, c.d, goff, dxr, hdr, s);
   if (e == cudaSuccess)
-    e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, W2T, W13T, dYb, pre, dact, dxd, R,
-                          hdr, s);
+    e = launch_router_dx_tc(dzb, c.T, B.kp, in->Wg, c.E, c.d, goff, dxr, hdr, s);
+  if (e == cudaSuccess)
+    e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, in->W2, W13T, dYb, pre, dact, dxd,
+                          R, hdr, s);
   if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s);
   if (e == cudaSuccess)
     e = launch_bwd_wg(c, dz, dzT, B.kp, in->x, at<void>(bws, B.xT), B.tp,

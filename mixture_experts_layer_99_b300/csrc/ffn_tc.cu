@@ -197,7 +197,11 @@ __device__ __forceinline__ TileInfo tile_info(const ST& st, const int32_t* __res
 // signals it remotely), issues the M = 256 MMAs and multicasts every commit
 // to both CTAs; each CTA's epilogue drains its own TMEM rows and releases the
 // accumulator on rank 0's `tmem_empty` (one arrive per warp).
-template <int MODE, bool SCATTER, bool PAIR, class PIPE>
+// BMN: B is read MN-major straight from a row-major [E, K, N] tensor (the
+// backward's dY W2 and dact [W1; W3] products, no transposed copy of the
+// weights): per stage, boxes of [64 K rows x 64 N] side by side; with kb3 <
+// num_kb the K blocks from kb3 on come from tmB3 (W3 after W1).
+template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
                            const int32_t* __restrict__ o_rows,
                            const float* __restrict__ o_scale,
-                           const __nv_bfloat16* __restrict__ pre, int ldo) {
+                           const __nv_bfloat16* __restrict__ pre, int ldo, int kb3) {
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
   constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu;
   constexpr int STAGES = PIPE::STAGES;
@@ -306,7 +310,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           uint8_t* a_dst = sA + stage * A_BYTES;
           uint8_t* b_dst = sB + stage * B_STAGE;
-          if (PAIR) {
+          if (PAIR && BMN) {
+            // B as two boxes of [64 K rows x 64 N] per CTA (half of N each)
+            const uint32_t bar = cluster_addr(&st.full[stage], 0);
+            if (rank == 0) mbar_expect_tx(&st.full[stage], TX_BYTES);
+            tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, a_row);
+            const CUtensorMap* mb = kb >= kb3 ? &tmB3 : &tmB;
+            const int kk = (kb >= kb3 ? kb - kb3 : kb) * BK;
+#pragma unroll
+            for (int ch = 0; ch < UMMA_N / 2 / 64; ++ch)
+              tma_load_3d_pair(b_dst + ch * (BK * 128), mb, bar,
+                               ti.n0 + (int)rank * (UMMA_N / 2) + 64 * ch, kk, ti.e);
+          } else if (PAIR) {
             const uint32_t bar = cluster_addr(&st.full[stage], 0);
             if (rank == 0) mbar_expect_tx(&st.full[stage], TX_BYTES);
             tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, a_row);
@@ -314,6 +329,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_3d_pair(b_dst, rank == 0 ? &tmB : &tmB3, bar, kb * BK, ti.n0, ti.e);
             else
               tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, ti.n0 + (int)rank * (UMMA_N / 2), ti.e);
+          } else if (BMN) {
+            // B as four boxes of [64 K rows x 64 N]
+            const CUtensorMap* mb = kb >= kb3 ? &tmB3 : &tmB;
+            const int kk = (kb >= kb3 ? kb - kb3 : kb) * BK;
+            constexpr int NCH = (PAIR ? UMMA_N / 2 : UMMA_N) / 64;
+            mbar_expect_tx(&st.full[stage], TX_BYTES);
+            tma_load_2d(a_dst, &tmA, &st.full[stage], kb * BK, a_row);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+              tma_load_3d(b_dst + ch * (BK * 128), mb, &st.full[stage], ti.n0 + 64 * ch, kk, ti.e);
           } else {
             mbar_expect_tx(&st.full[stage], TX_BYTES);
             tma_load_2d(a_dst, &tmA, &st.full[stage], kb * BK, a_row);
@@ -358,7 +383,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ================= MMA issuer (rank 0 of a pair)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM_T, UMMA_N);
+      constexpr uint32_t IDESC =
+          BMN ? idesc_bf16_f32_bmn(BM_T, UMMA_N) : idesc_bf16_f32(BM_T, UMMA_N);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -380,17 +406,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sdesc_kmajor_sw128(a0 + stage * A_BYTES);
-          const uint64_t bdesc = sdesc_kmajor_sw128(b0 + stage * B_STAGE);
+          const uint64_t bdesc = BMN ? sdesc_mnmajor_sw128(b0 + stage * B_STAGE, BK * 128)
+                                     : sdesc_kmajor_sw128(b0 + stage * B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // advance along K inside the 128-byte swizzle row: 16 bf16 = 32 B
+            // advance along K: K-major inside the 128-byte swizzle row (16 bf16
+            // = 32 B), MN-major by two 8-row swizzle atoms (2048 B)
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t bstep = BMN ? (uint64_t)(kk * 128) : (uint64_t)(kk * 2);
             if (PAIR)
-              umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2),
-                             IDESC, accum);
+              umma_bf16_pair(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + bstep, IDESC, accum);
             else
-              umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), IDESC,
-                        accum);
+              umma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + bstep, IDESC, accum);
           }
           if (PAIR) umma_commit_pair(&st.empty[stage]);
           else umma_commit(&st.empty[stage]);
@@ -678,14 +705,14 @@ bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool SCATTER, bool PAIR, class PIPE>
+template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN>
 cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                           const CUtensorMap& o, const int32_t* offset, int E, int N, int K,
                           const void* bias, void* out, int64_t rows_bound, int32_t* hdr,
                           const int32_t* o_rows, const float* o_scale, const void* pre,
-                          int ldo, cudaStream_t s) {
+                          int ldo, int kb3, cudaStream_t s) {
   constexpr size_t SMEM_BYTES = smem_bytes<PAIR, PIPE>();
-  auto kernel = grouped_gemm_tc_kernel<MODE, SCATTER, PAIR, PIPE>;
+  auto kernel = grouped_gemm_tc_kernel<MODE, SCATTER, PAIR, PIPE, BMN>;
   static int max_units[64] = {};  // per device: CTAs (or CTA pairs) resident at once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -722,21 +749,24 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   return launch_pdl_cluster(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
                             b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
                             static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale,
-                            static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N);
+                            static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N, kb3);
 }
 
-template <int MODE, bool SCATTER>
+// BMN (B MN-major): kb3 is the first K block read through b3 (< 0: none).
+template <int MODE, bool SCATTER, bool BMN = false>
 cudaError_t launch_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& b3, const CUtensorMap& o, const int32_t* offset, int E,
                         int N, int K, const void* bias, void* out, int64_t rows_bound,
                         int32_t* hdr, const int32_t* o_rows, const float* o_scale,
-                        cudaStream_t s, const void* pre = nullptr, int ldo = 0) {
+                        cudaStream_t s, const void* pre = nullptr, int ldo = 0, int kb3 = -1) {
+  if (!BMN || kb3 < 0) kb3 = (K + BK - 1) / BK;
   if (pair)
-    return launch_gemm_p<MODE, SCATTER, true, PipePairShape>(
-        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, s);
-  return launch_gemm_p<MODE, SCATTER, false, PipeShape>(a, b, b3, o, offset, E, N, K, bias, out,
-                                                        rows_bound, hdr, o_rows, o_scale, pre,
-                                                        ldo, s);
+    return launch_gemm_p<MODE, SCATTER, true, PipePairShape, BMN>(
+        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, kb3,
+        s);
+  return launch_gemm_p<MODE, SCATTER, false, PipeShape, BMN>(a, b, b3, o, offset, E, N, K, bias,
+                                                             out, rows_bound, hdr, o_rows,
+                                                             o_scale, pre, ldo, kb3, s);
 }
 
 }  // namespace
@@ -749,7 +779,7 @@ static bool pairs_fit() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (fit[dev] == 0) {
-    auto kernel = grouped_gemm_tc_kernel<kPlain, false, true, PipePairShape>;
+    auto kernel = grouped_gemm_tc_kernel<kPlain, false, true, PipePairShape, false>;
     constexpr size_t SMEM_BYTES = smem_bytes<true, PipePairShape>();
     int n = 0;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -829,7 +859,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
 // weights (K-major operands); the pre-activations are recomputed here rather
 // than kept from the forward pass.
 cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
-                              const void* W1, const void* W3, const void* b1, const void* W2T,
+                              const void* W1, const void* W3, const void* b1, const void* W2,
                               const void* W13T, const void* dY, void* pre, void* dact,
                               void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
   const uint64_t R = (uint64_t)rows_bound;
@@ -837,12 +867,11 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
   const bool pair = use_pairs(c);
   const uint64_t H = (uint64_t)c.H, d = (uint64_t)c.d, Hp = swiglu ? 2 * H : H;
   const uint32_t box = pair ? 128 : UMMA_N;
-  CUtensorMap mxd, mw1, mw3, mpa, mpv, mdy, mw2t, mdact_o, mdact_a, mw13t, mdxd;
+  CUtensorMap mxd, mw1, mw3, mpa, mpv, mdy, mw2n, mdact_o, mdact_a, mdxd;
   if (!make_map_2d(&mxd, xd, d, R) || !make_map_3d(&mw1, W1, d, H, c.E, box) ||
       !make_map_out(&mpa, pre, H, R, Hp) || !make_map_2d(&mdy, dY, d, R) ||
-      !make_map_3d(&mw2t, W2T, d, H, c.E, box) || !make_map_out(&mdact_o, dact, Hp, R) ||
-      !make_map_2d(&mdact_a, dact, Hp, R) || !make_map_3d(&mw13t, W13T, Hp, d, c.E, box) ||
-      !make_map_out(&mdxd, dxd, d, R))
+      !make_map_3d(&mw2n, W2, H, d, c.E, BK) || !make_map_out(&mdact_o, dact, Hp, R) ||
+      !make_map_2d(&mdact_a, dact, Hp, R) || !make_map_out(&mdxd, dxd, d, R))
     return cudaErrorInvalidValue;
   cudaError_t e;
   // recomputed pre-activations
@@ -859,32 +888,44 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
                                    nullptr, s, nullptr, (int)Hp);
     if (e != cudaSuccess) return e;
   }
-  // dh = dY W2, times the activation's derivative
+  // dh = dY W2 (W2 [E, d, H] read MN-major), times the activation's derivative
   if (swiglu)
-    e = launch_gemm<kBwdSwiglu, false>(pair, mdy, mw2t, mw2t, mdact_o, offset, c.E, c.H, c.d,
-                                       nullptr, dact, rows_bound, hdr, nullptr, nullptr, s, pre,
-                                       (int)Hp);
+    e = launch_gemm<kBwdSwiglu, false, true>(pair, mdy, mw2n, mw2n, mdact_o, offset, c.E, c.H,
+                                             c.d, nullptr, dact, rows_bound, hdr, nullptr,
+                                             nullptr, s, pre, (int)Hp);
   else
-    e = launch_gemm<kBwdGelu, false>(pair, mdy, mw2t, mw2t, mdact_o, offset, c.E, c.H, c.d,
-                                     nullptr, dact, rows_bound, hdr, nullptr, nullptr, s, pre);
+    e = launch_gemm<kBwdGelu, false, true>(pair, mdy, mw2n, mw2n, mdact_o, offset, c.E, c.H, c.d,
+                                           nullptr, dact, rows_bound, hdr, nullptr, nullptr, s,
+                                           pre);
   if (e != cudaSuccess) return e;
-  // dxd = dact [W1; W3]
+  // dxd = dact [W1; W3]: W1 (and W3) [E, H, d] read MN-major, W3's K blocks
+  // after W1's; a SwiGLU hidden size that is not a multiple of 64 would put
+  // one K block across both, so that case reads the transposed copy W13T
+  if (!bwd_w13_transposed(c)) {
+    CUtensorMap mw1n, mw3n;
+    if (!make_map_3d(&mw1n, W1, d, H, c.E, BK) ||
+        !make_map_3d(&mw3n, swiglu ? W3 : W1, d, H, c.E, BK))
+      return cudaErrorInvalidValue;
+    return launch_gemm<kPlain, false, true>(pair, mdact_a, mw1n, mw3n, mdxd, offset, c.E, c.d,
+                                            (int)Hp, nullptr, dxd, rows_bound, hdr, nullptr,
+                                            nullptr, s, nullptr, 0,
+                                            swiglu ? (int)(H / BK) : -1);
+  }
+  CUtensorMap mw13t;
+  if (!W13T || !make_map_3d(&mw13t, W13T, Hp, d, c.E, box)) return cudaErrorInvalidValue;
   return launch_gemm<kPlain, false>(pair, mdact_a, mw13t, mw13t, mdxd, offset, c.E, c.d,
                                     (int)Hp, nullptr, dxd, rows_bound, hdr, nullptr, nullptr, s);
 }
-
-// Router part of dx in the backward pass: dxr [T, d] = dz [T, Kp] WgT^T with
-// dz in bf16 and the experts zero-padded to Kp (a multiple of 64), WgT [d, Kp]
-// the transposed router weight, one group over all T rows (off = [0, T]).
-cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* WgT, int d,
+cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* Wg, int E, int d,
                                 const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s) {
+  // W_g [E, d] read MN-major as [K = E (zero beyond E), N = d]
   CUtensorMap ma, mb, mo;
   if (!make_map_2d(&ma, dz_bf16, (uint64_t)Kp, (uint64_t)T) ||
-      !make_map_3d(&mb, WgT, (uint64_t)Kp, (uint64_t)d, 1, UMMA_N) ||
+      !make_map_3d(&mb, Wg, (uint64_t)d, (uint64_t)E, 1, BK) ||
       !make_map_out(&mo, dxr, (uint64_t)d, (uint64_t)T))
     return cudaErrorInvalidValue;
-  return launch_gemm<kPlain, false>(false, ma, mb, mb, mo, off, 1, d, Kp, nullptr, dxr, T, hdr,
-                                    nullptr, nullptr, s);
+  return launch_gemm<kPlain, false, true>(false, ma, mb, mb, mo, off, 1, d, Kp, nullptr, dxr, T,
+                                          hdr, nullptr, nullptr, s);
 }
 
 }  // namespace moe

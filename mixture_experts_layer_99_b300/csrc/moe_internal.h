@@ -199,11 +199,17 @@ cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* 
 cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s);
 
 // ---- backward pass
+// The backward GEMMs read the weights in their stored layout (B MN-major);
+// only a SwiGLU hidden size that is not a multiple of 64 needs the
+// transposed copy W13T = [W1^T | W3^T] per expert for dxd = dact [W1; W3].
+inline bool bwd_w13_transposed(const moe_config_t& c) {
+  return c.act == MOE_ACT_SWIGLU && c.H % 64 != 0;
+}
 cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
-                              const void* W1, const void* W3, const void* b1, const void* W2T,
+                              const void* W1, const void* W3, const void* b1, const void* W2,
                               const void* W13T, const void* dY, void* pre, void* dact,
                               void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s);
-cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* WgT, int d,
+cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* Wg, int E, int d,
                                 const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s);
 cudaError_t launch_wgrad_tc(const void* At, const void* Bt, int64_t ld, const int32_t* poff,
                             int E, int M, int N, int m_split, float* out, float* out2,

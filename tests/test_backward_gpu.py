@@ -30,6 +30,8 @@ CASES = {
     "sweep_small": (W.small(WL["sweep_e16_k4"], T=2048, d=256, H=512), 0.1, True),
     "drops_heavy": (W.small(WL["longtail"], T=999, d=64, H=64, c=Fraction(1, 3)), 0.2, False),
     "ragged_dims": (W.small(WL["switch_top1"], T=600, d=136, H=200, E=5, k=2), 0.3, True),
+    # SwiGLU with H not a multiple of 64: dxd reads the transposed [W1^T | W3^T]
+    "swiglu_ragged_h": (W.small(WL["mixtral"], T=640, d=136, H=200, E=5), 0.1, False),
 }
 
 
