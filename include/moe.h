@@ -301,9 +301,10 @@ MOE_API moe_status_t moe_workspace_size_backward(const moe_config_t *cfg, size_t
  * after the forward, with the same cfg, in, ws and outputs `fwd`, before
  * anything else reuses ws: it reads the forward's routing (fwd->logits,
  * topk_idx, topk_gate, slot_of, expert_offset and f must all be non-NULL),
- * the gathered rows and, for k > 1, the expert outputs kept in ws. dy [T, d]
- * is the upstream gradient of y (layer dtype); alpha the weight of
- * L_balance. The expert pre-activations are recomputed. Every sum is taken in
+ * the gathered rows, the expert hidden activations h and, for k > 1, the
+ * expert outputs kept in ws. dy [T, d] is the upstream gradient of y (layer
+ * dtype); alpha the weight of L_balance. The expert pre-activations are
+ * recomputed (for the activation's derivative). Every sum is taken in
  * a fixed order (results are run-to-run identical). Covered: bf16 with
  * E <= 64 (the tensor-core forward); no shared expert. Nothing is enqueued
  * on a validation failure. */

@@ -465,19 +465,14 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {
-  size_t hdr, pre, dact, dY, dxd, poff, tdY, th, tdact, txd, W13T, dz, dg, wg_part, dzb, dxr,
-      goff, dzT, xT, wgoff, total;
-  int kp;      // experts padded to a multiple of 64 (K of the dz W_g GEMM)
-  int tp;      // tokens padded to a multiple of 64 (K of the dz^T x GEMM)
-  int64_t rp;  // padded packed-row bound (columns of the transposed operands)
+  size_t hdr, pre, dact, dY, dxd, W13T, dz, dg, wg_part, dzb, dxr, goff, wgoff, total;
+  int kp;  // experts padded to a multiple of 64 (K of the dz W_g GEMM)
 };
 BwdLayout bwd_layout(const moe_config_t& c) {
   BwdLayout L;
   memset(&L, 0, sizeof(L));
   const size_t R = (size_t)max_rows(c), E = (size_t)c.E, d = (size_t)c.d, H = (size_t)c.H;
   const size_t Hp = c.act == MOE_ACT_SWIGLU ? 2 * H : H;
-  L.rp = (int64_t)align_up(R + 64 * E, 64);
-  const size_t rp = (size_t)L.rp;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -489,19 +484,11 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.dact = take(R * Hp * 2);
   L.dY = take(R * d * 2);
   L.dxd = take(R * d * 2);
-  L.poff = take((E + 1) * 4);
-  L.tdY = take(d * rp * 2);
-  L.th = take(H * rp * 2);
-  L.tdact = take(Hp * rp * 2);
-  L.txd = take(d * rp * 2);
   L.W13T = take(bwd_w13_transposed(c) ? E * d * Hp * 2 : 0);
   L.dz = take((size_t)c.T * E * 4);
   L.dg = take((size_t)c.T * (size_t)c.k * 4);
   L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
   L.kp = (int)align_up(E, 64);
-  L.tp = (int)align_up((size_t)c.T, 64);
-  L.dzT = take((size_t)L.kp * (size_t)L.tp * 2);
-  L.xT = take(d * (size_t)L.tp * 2);
   L.wgoff = take(((size_t)bwd_wg_splits(c) + 1) * 4);
   L.dzb = take((size_t)c.T * (size_t)L.kp * 2);
   L.dxr = take((size_t)c.T * d * 2);
@@ -556,11 +543,9 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   void* dact = at<void>(bws, B.dact);
   void* dYb = at<void>(bws, B.dY);
   void* dxd = at<void>(bws, B.dxd);
-  int32_t* poff = at<int32_t>(bws, B.poff);
   void* W13T = bwd_w13_transposed(c) ? at<void>(bws, B.W13T) : nullptr;
   float* dz = at<float>(bws, B.dz);
   float* dg = at<float>(bws, B.dg);
-  const int ldp = (int)B.rp;
   cudaError_t e = cudaSuccess;
   if (W13T) {
     e = launch_weight_transpose(in->W1, c.E, c.H, c.d, Hp, 0, W13T, s);
@@ -570,11 +555,9 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   void* dzb = at<void>(bws, B.dzb);
   void* dxr = at<void>(bws, B.dxr);
   int32_t* goff = at<int32_t>(bws, B.goff);
-  void* dzT = at<void>(bws, B.dzT);
-  if (e == cudaSuccess) e = cudaMemsetAsync(dzT, 0, (size_t)B.kp * B.tp * 2, s);
   if (e == cudaSuccess)
     e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz,
-                          dzb, B.kp, dzT, B.tp, s);
+                          dzb, B.kp, s);
   // router part of dx on the tensor cores: dxr = dz W_g (experts zero-padded)
   if (e == cudaSuccess) e = launch_one_group_offsets(goff, c.T, s);
   if (e == cudaSuccess)
@@ -584,26 +567,16 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
                           R, hdr, s);
   if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s);
   if (e == cudaSuccess)
-    e = launch_bwd_wg(c, dz, dzT, B.kp, in->x, at<void>(bws, B.xT), B.tp,
-                      at<int32_t>(bws, B.wgoff), at<float>(bws, B.wg_part), g->dWg, g->dbias, hdr,
-                      s);
-  if (e == cudaSuccess) e = launch_pad_offsets(off, c.E, poff, s);
+    e = launch_bwd_wg(c, dz, dzb, B.kp, in->x, at<int32_t>(bws, B.wgoff),
+                      at<float>(bws, B.wg_part), g->dWg, g->dbias, hdr, s);
+  // dW2 [E, d, H] = dY^T h (h as the forward left it in its workspace);
+  // [dW1; dW3] [E, Hp, d] = dact^T xd; row-major operands read MN-major
   if (e == cudaSuccess)
-    e = launch_transpose_pad(0, dYb, c.d, c.d, off, poff, c.E, B.rp, at<void>(bws, B.tdY), ldp, s);
-  if (e == cudaSuccess)
-    e = launch_transpose_pad(swiglu ? 2 : 1, pre, Hp, c.H, off, poff, c.E, B.rp,
-                             at<void>(bws, B.th), ldp, s);
-  if (e == cudaSuccess)
-    e = launch_transpose_pad(0, dact, Hp, Hp, off, poff, c.E, B.rp, at<void>(bws, B.tdact), ldp, s);
-  if (e == cudaSuccess)
-    e = launch_transpose_pad(0, xd, c.d, c.d, off, poff, c.E, B.rp, at<void>(bws, B.txd), ldp, s);
-  // dW2 [E, d, H] = dY^T h;  [dW1; dW3] [E, Hp, d] = dact^T xd
-  if (e == cudaSuccess)
-    e = launch_wgrad_tc(at<void>(bws, B.tdY), at<void>(bws, B.th), B.rp, poff, c.E, c.d, c.H, c.d,
+    e = launch_wgrad_tc(dYb, c.d, at<void>(wsm, L.ffn_h), c.H, R, off, c.E, c.d, c.H, c.d,
                         g->dW2, g->dW2, hdr, s);
   if (e == cudaSuccess)
-    e = launch_wgrad_tc(at<void>(bws, B.tdact), at<void>(bws, B.txd), B.rp, poff, c.E, Hp, c.d,
-                        c.H, g->dW1, swiglu ? g->dW3 : g->dW1, hdr, s);
+    e = launch_wgrad_tc(dact, Hp, xd, c.d, R, off, c.E, Hp, c.d, c.H, g->dW1,
+                        swiglu ? g->dW3 : g->dW1, hdr, s);
   if (e == cudaSuccess && g->db1) e = launch_expert_colsum(dact, Hp, c.H, off, c.E, g->db1, s);
   if (e == cudaSuccess && g->db2) e = launch_expert_colsum(dYb, c.d, c.d, off, c.E, g->db2, s);
   return cuda_status(e);

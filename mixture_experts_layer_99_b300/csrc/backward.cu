@@ -81,8 +81,7 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ idx,
     const float* __restrict__ gate, const float* __restrict__ dg,
     const float* __restrict__ f, float alpha, float tau, int T, int E, int k,
-    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp,
-    __nv_bfloat16* __restrict__ dzT, int Tp) {
+    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float p[EP];
@@ -135,10 +134,8 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
     if (e < E) dz[(size_t)t * E + e] = z;
     dp[e] = z;
   }
-  // transposed bf16 copy [Kp][Tp] (the operand of the dz^T x GEMM)
-#pragma unroll
-  for (int e = 0; e < EP; ++e) dzT[(size_t)e * Tp + t] = __float2bfloat16_rn(dp[e]);
-  // bf16 copy with the experts padded to Kp (the operand of the dz W_g GEMM)
+  // bf16 copy with the experts padded to Kp (the operand of the dz W_g and
+  // dz^T x GEMMs)
   __nv_bfloat16* zr = dzb + (size_t)t * Kp;
   for (int e0 = 0; e0 < Kp; e0 += 8) {
     float v[8];
@@ -234,80 +231,8 @@ __global__ void bwd_wg_reduce_kernel(const float* __restrict__ part, int nsplit,
   }
 }
 
-// Padded expert offsets: poff_0 = 0, poff_{e+1} = poff_e + roundup(rows_e, 64).
-__global__ void pad_offsets_kernel(const int32_t* __restrict__ off, int E,
-                                   int32_t* __restrict__ poff) {
-  if (threadIdx.x != 0) return;
-  int run = 0;
-  poff[0] = 0;
-  for (int e = 0; e < E; ++e) {
-    const int n = off[e + 1] - off[e];
-    run += (n + 63) / 64 * 64;
-    poff[e + 1] = run;
-  }
-}
-
-// out[c, p] = act(in rows) transposed into the padded expert layout: packed
-// row r of expert e (r in [off_e, off_{e+1})) goes to column
-// poff_e + (r - off_e); the columns up to the next multiple of 64 are zero.
-// ACT 0: copy of in[:, c]; 1: gelu(in[:, c]); 2: silu(in[:, c]) * in[:, C + c]
-// (the SwiGLU hidden row from the packed [gate | up] pre-activations).
-// Block = 64 padded columns x 64 channels, moved as 16-byte vectors (C, the
-// strides and the channel offsets are multiples of 8); a 64-column block
-// never straddles two experts because every poff_e is a multiple of 64.
-template <int ACT>
-__global__ void __launch_bounds__(256) transpose_pad_kernel(
-    const __nv_bfloat16* __restrict__ in, int ld_in, int C, const int32_t* __restrict__ off,
-    const int32_t* __restrict__ poff, int E, __nv_bfloat16* __restrict__ out, int ld_out) {
-  __shared__ __align__(16) __nv_bfloat16 tile[64][72];  // [row i][channel j]
-  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-  if (p0 >= poff[E]) return;
-  int lo = 0, hi = E - 1;  // expert with poff_e <= p0 < poff_{e+1}
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (poff[mid] <= p0) lo = mid;
-    else hi = mid - 1;
-  }
-  const int e = lo;
-  const int local = p0 - poff[e];
-  const int nvalid = min(64, off[e + 1] - off[e] - local);
-  const int r0 = off[e] + local;
-  const int tid = threadIdx.x;
-  // load: 64 rows x 8 vectors of 8 channels
-  for (int q = tid; q < 64 * 8; q += 256) {
-    const int i = q >> 3, jv = q & 7;
-    const int c = c0 + jv * 8;
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (i < nvalid && c < C) {
-      const __nv_bfloat16* rp = in + (size_t)(r0 + i) * ld_in;
-      unpack8(__ldg(reinterpret_cast<const uint4*>(rp + c)), v);
-      if (ACT == 1) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = 0.5f * v[t] * (1.f + erff(v[t] * 0.70710678118654752f));
-      } else if (ACT == 2) {
-        float u[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(rp + C + c)), u);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = v[t] / (1.f + expf(-v[t])) * u[t];
-      }
-    }
-    *reinterpret_cast<uint4*>(&tile[i][jv * 8]) = pack8(v);
-  }
-  __syncthreads();
-  // store: channel j, 8 consecutive padded columns per 16-byte vector
-  for (int q = tid; q < 64 * 8; q += 256) {
-    const int j = q & 63, iv = q >> 6;
-    const int c = c0 + j;
-    if (c >= C) continue;
-    uint4 w;
-    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&w);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) h[t] = tile[iv * 8 + t][j];
-    *reinterpret_cast<uint4*>(out + (size_t)c * ld_out + p0 + iv * 8) = w;
-  }
-}
-
-// Batched transpose of expert weights: out[e][b][a + a_off] = in[e][a][b]
+// Batched transpose of expert weights (the [W1^T | W3^T] copy a SwiGLU hidden
+// size that is not a multiple of 64 needs): out[e][b][a + a_off] = in[e][a][b]
 // (in [E, A, B] row-major, out [E, B, ld_out]); 64 x 64 tiles moved as
 // 16-byte vectors (A, B, ld_out and a_off are multiples of 8).
 __global__ void __launch_bounds__(256) weight_transpose_kernel(
@@ -356,10 +281,10 @@ __global__ void __launch_bounds__(128) expert_colsum_kernel(const __nv_bfloat16*
 template <int EP>
 cudaError_t launch_router_bwd_ep(const moe_config_t& c, const float* logits, const int32_t* idx,
                                  const float* gate, const float* dg, const float* f, float alpha,
-                                 float* dz, void* dzb, int Kp, void* dzT, int Tp, cudaStream_t s) {
+                                 float* dz, void* dzb, int Kp, cudaStream_t s) {
   bwd_router_kernel<EP><<<(c.T + 127) / 128, 128, 0, s>>>(
       logits, idx, gate, dg, f, alpha, c.tau, c.T, c.E, c.k, dz,
-      static_cast<__nv_bfloat16*>(dzb), Kp, static_cast<__nv_bfloat16*>(dzT), Tp);
+      static_cast<__nv_bfloat16*>(dzb), Kp);
   return cudaGetLastError();
 }
 
@@ -392,10 +317,10 @@ cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void
 
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, void* dzb, int Kp, void* dzT, int Tp, cudaStream_t s) {
+                              float* dz, void* dzb, int Kp, cudaStream_t s) {
   const int ep = (c.E + 15) / 16 * 16;
 #define MOE_RB(EPV) \
-  launch_router_bwd_ep<EPV>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, dzT, Tp, s)
+  launch_router_bwd_ep<EPV>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s)
   switch (ep) {
     case 16: return MOE_RB(16);
     case 32: return MOE_RB(32);
@@ -417,22 +342,18 @@ cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t*
 }
 
 // dWg = dz^T x on the tensor cores: token groups of the weight-gradient GEMM
-// (At = dz^T [Kp][Tp], Bt = x^T [d][Tp]) give fp32 partials [G][E][d], summed
-// in group order; db = column sums of dz.
-cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzT, int Kp,
-                          const void* x, void* xT, int Tp, int32_t* goff, float* part,
-                          float* dWg, float* dbias, int32_t* hdr, cudaStream_t s) {
+// (A = dz in bf16 [T][Kp], B = x [T][d], both read MN-major; groups are
+// multiples of 64 tokens, rows past T read as zeros) give fp32 partials
+// [G][E][d], summed in group order; db = column sums of dz.
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzb, int Kp,
+                          const void* x, int32_t* goff, float* part, float* dWg, float* dbias,
+                          int32_t* hdr, cudaStream_t s) {
   const int G = bwd_wg_splits(c), per = bwd_wg_group_tokens(c);
-  (void)Kp;
-  const int t8 = (c.T + 7) / 8 * 8;
-  cudaError_t e = launch_weight_transpose(x, 1, c.T, c.d, Tp, 0, xT, s);
-  if (e == cudaSuccess && Tp > t8)
-    e = cudaMemset2DAsync(static_cast<__nv_bfloat16*>(xT) + t8, (size_t)Tp * 2, 0,
-                          (size_t)(Tp - t8) * 2, (size_t)c.d, s);
-  if (e != cudaSuccess) return e;
+  const int Tp = (c.T + 63) / 64 * 64;
   group_offsets_kernel<<<1, 128, 0, s>>>(goff, G, per, Tp);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = launch_wgrad_tc(dzT, xT, Tp, goff, G, c.E, c.d, c.E, part, part, hdr, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_wgrad_tc(dzb, Kp, x, c.d, c.T, goff, G, c.E, c.d, c.E, part, part, hdr, s);
   if (e != cudaSuccess) return e;
   const int n = c.E * c.d;
   bwd_wg_reduce_kernel<<<(n + 255) / 256, 256, 0, s>>>(part, G, c.E, c.d, dWg);
@@ -444,22 +365,6 @@ cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dz
   return e;
 }
 
-cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s) {
-  pad_offsets_kernel<<<1, 32, 0, s>>>(off, E, poff);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_pad(int act, const void* in, int ld_in, int C, const int32_t* off,
-                                 const int32_t* poff, int E, int64_t rp_bound, void* out,
-                                 int ld_out, cudaStream_t s) {
-  const dim3 grid((unsigned)((rp_bound + 63) / 64), (unsigned)((C + 63) / 64));
-  const __nv_bfloat16* i = static_cast<const __nv_bfloat16*>(in);
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  if (act == 0) transpose_pad_kernel<0><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
-  else if (act == 1) transpose_pad_kernel<1><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
-  else transpose_pad_kernel<2><<<grid, 256, 0, s>>>(i, ld_in, C, off, poff, E, o, ld_out);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_weight_transpose(const void* in, int E, int A, int B, int ld_out, int a_off,
                                     void* out, cudaStream_t s) {

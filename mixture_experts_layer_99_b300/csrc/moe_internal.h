@@ -211,27 +211,22 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
                               void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s);
 cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* Wg, int E, int d,
                                 const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s);
-cudaError_t launch_wgrad_tc(const void* At, const void* Bt, int64_t ld, const int32_t* poff,
-                            int E, int M, int N, int m_split, float* out, float* out2,
-                            int32_t* hdr, cudaStream_t s);
+cudaError_t launch_wgrad_tc(const void* A, int64_t lda, const void* B, int64_t ldb,
+                            int64_t rows, const int32_t* off, int E, int M, int N, int m_split,
+                            float* out, float* out2, int32_t* hdr, cudaStream_t s);
 int bwd_wg_splits(const moe_config_t& c);
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
                                const int32_t* slot_of, const float* gate, void* dY, float* dg,
                                cudaStream_t s);
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
-                              float* dz, void* dz_bf16, int Kp, void* dzT, int Tp,
-                              cudaStream_t s);
+                              float* dz, void* dz_bf16, int Kp, cudaStream_t s);
 int bwd_wg_group_tokens(const moe_config_t& c);
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
                           const void* dxr, void* dx, cudaStream_t s);
-cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzT, int Kp,
-                          const void* x, void* xT, int Tp, int32_t* goff, float* part,
-                          float* dWg, float* dbias, int32_t* hdr, cudaStream_t s);
-cudaError_t launch_pad_offsets(const int32_t* off, int E, int32_t* poff, cudaStream_t s);
-cudaError_t launch_transpose_pad(int act, const void* in, int ld_in, int C, const int32_t* off,
-                                 const int32_t* poff, int E, int64_t rp_bound, void* out,
-                                 int ld_out, cudaStream_t s);
+cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzb, int Kp,
+                          const void* x, int32_t* goff, float* part, float* dWg, float* dbias,
+                          int32_t* hdr, cudaStream_t s);
 cudaError_t launch_weight_transpose(const void* in, int E, int A, int B, int ld_out, int a_off,
                                     void* out, cudaStream_t s);
 cudaError_t launch_expert_colsum(const void* a, int ld, int C, const int32_t* off, int E,
