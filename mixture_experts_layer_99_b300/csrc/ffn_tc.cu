@@ -855,9 +855,10 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
 //   pre  = xd W1^T (+ b1) [R, H]      (SwiGLU: [a | v] = xd [W1; W3]^T, [R, 2H])
 //   dact = (dY W2) * act'(pre)        [R, H]  (SwiGLU: [d gate | d up], [R, 2H])
 //   dxd  = dact W1                    [R, d]  (SwiGLU: [d gate | d up] [W1; W3])
-// W2T [E, H, d] and W13T [E, d, Hp] (Hp = H or 2H) are the transposed expert
-// weights (K-major operands); the pre-activations are recomputed here rather
-// than kept from the forward pass.
+// The weights are read as stored (W2 [E, d, H], W1 and W3 [E, H, d]: B
+// MN-major); W13T [E, d, Hp] (Hp = 2H), the transposed [W1; W3], is used only
+// by a SwiGLU hidden size that is not a multiple of 64 (else NULL). The
+// pre-activations are recomputed here rather than kept from the forward pass.
 cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                               const void* W1, const void* W3, const void* b1, const void* W2,
                               const void* W13T, const void* dY, void* pre, void* dact,
