@@ -23,8 +23,8 @@ section:
   sections 2.2 and 3.3 (Gumbel noise added to the logits before the softmax,
   temperature division).
 
-Readings where the pages are silent or disagree (each listed in the design
-notes of the repository):
+Readings where the pages are silent or disagree (the section each reading
+rests on is named with it):
 
 * Selection is on the logits, ties go to the lower expert index, and the k
   chosen experts are ordered by descending logit ([MoE-math] 2.1 says to pick
@@ -251,7 +251,10 @@ def balance_from_sums(count, prob_sum, T: int, k: int, kept):
 
 def combine_rows(Yrows, slot_of, gates):
     """Combine step alone: y_t = sum over j with slot_of[t,j] >= 0 of
-    g[t,j] * Yrows[slot_of[t,j]] (fp64), y_t = 0 if no slot was kept."""
+    g[t,j] * Yrows[slot_of[t,j]] (fp64), y_t = 0 if no slot was kept.
+    Pinned: fed the packed outputs of each expert on its kept rows, it
+    reproduces the layer's y, which the dense-masked loop and the sort-based
+    restatement pin on their own (tests)."""
     Yrows = as_f64(Yrows)
     slot_of = np.asarray(slot_of)
     gates = np.asarray(gates, dtype=np.float64)

@@ -339,6 +339,40 @@ def pin_dropped_tokens_zero(o):
     assert r["dropped"] == k * (T - 5)
 
 
+def pin_combine_rows_is_layer_output(o):
+    """The combine step alone, fed the packed expert outputs, equals the
+    layer's y (y = sum_j g_j E_{K_j}(x) with dropped slots masked; kwkr.cn MoE
+    article, sections 2.1 and 2.3). The layer's y is pinned independently by
+    the dense-masked loop and the sort-based restatement, so a combine that
+    ignores the gates, keeps dropped slots or reads the wrong packed row fails
+    here. Cases with drops, k = 2 and k = 3, and one token-ordered tie so that
+    dropped and kept slots sit side by side."""
+    rng = _rng(12)
+    for act, T, E, k, c in (("gelu", 37, 5, 2, Fraction(3, 5)),
+                            ("swiglu", 29, 6, 3, Fraction(1, 2)),
+                            ("gelu", 16, 4, 2, Fraction(1, 4))):
+        d, H = 9, 13
+        x = rng.standard_normal((T, d))
+        Wg = rng.standard_normal((E, d))
+        W1, W3, W2, b1, b2 = _weights(rng, E, d, H, act == "swiglu", act == "gelu")
+        inp = dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, b1=b1, b2=b2)
+        r = o.moe_forward(inp, k=k, c=c, act=act)
+        assert r["dropped"] > 0 and (r["slot_of"] >= 0).any()
+        off = r["offset"]
+        Yrows = np.zeros((int(off[-1]), d))
+        for e in range(E):
+            a, b = int(off[e]), int(off[e + 1])
+            if b > a:
+                toks = r["token_of_row"][a:b]
+                Yrows[a:b] = _torch_ffn(x[toks], W1[e], None if W3 is None else W3[e], W2[e],
+                                        None if b1 is None else b1[e],
+                                        None if b2 is None else b2[e], act)
+        y = o.combine_rows(Yrows, r["slot_of"], r["gates"])
+        np.testing.assert_allclose(y, r["y"], rtol=0, atol=1e-12)
+        dead = (r["slot_of"] < 0).all(axis=1)
+        assert (y[dead] == 0).all()
+
+
 def pin_activations_match_library(o):
     u = np.linspace(-8, 8, 1001)
     ut = torch.from_numpy(u)
@@ -502,6 +536,21 @@ def _mutants():
         return o.__dict__["_orig_combine"](tokens, x, ids, gates, np.abs(np.asarray(slot_of)), *a, **kw)
     m["combine_keeps_dropped"] = ("combine_tokens", combine_keeps_dropped)
 
+    def combine_rows_no_gate(Yrows, slot_of, gates):
+        return o.__dict__["_orig_combine_rows"](Yrows, slot_of,
+                                                np.ones_like(np.asarray(gates, float)))
+    m["combine_rows_ignores_gates"] = ("combine_rows", combine_rows_no_gate)
+
+    def combine_rows_keeps_dropped(Yrows, slot_of, gates):
+        return o.__dict__["_orig_combine_rows"](Yrows, np.abs(np.asarray(slot_of)), gates)
+    m["combine_rows_keeps_dropped"] = ("combine_rows", combine_rows_keeps_dropped)
+
+    def combine_rows_next_row(Yrows, slot_of, gates):
+        s = np.asarray(slot_of)
+        n = np.asarray(Yrows).shape[0]
+        return o.__dict__["_orig_combine_rows"](Yrows, np.where(s >= 0, (s + 1) % n, s), gates)
+    m["combine_rows_wrong_row"] = ("combine_rows", combine_rows_next_row)
+
     def softmax_no_max_over_wrong_axis(l):
         e = np.exp(np.asarray(l, float))
         return e / e.sum(axis=0, keepdims=True)
@@ -526,7 +575,7 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     originals = dict(_orig_topk=o.topk_ids, _orig_dispatch=o.dispatch,
                      _orig_aux=o.aux_stats, _orig_ffn=o.expert_ffn_rows,
                      _orig_logits=o.router_logits, _orig_combine=o.combine_tokens,
-                     _orig_shared=o.shared_expert_rows)
+                     _orig_shared=o.shared_expert_rows, _orig_combine_rows=o.combine_rows)
     for k, v in originals.items():
         monkeypatch.setattr(o, k, v, raising=False)
     attr, bad = MUTANTS[name]
