@@ -118,11 +118,16 @@ def gate_logit_grads(p, ids, gates, dg, f, alpha: float, tau: float = 1.0):
 
 
 def moe_backward(inp: dict, k: int, c, act: str, dy, alpha: float = 0.0, tau: float = 1.0,
-                 logits=None, shared=None):
+                 logits=None, shared=None, noise_scale: float = 0.0):
     """Gradients of loss = sum <dy, y> + alpha * L_balance with respect to x,
     Wg, the router bias (if present), W1, W3, W2, b1, b2 (if present) and the
     shared expert's weights (if present). Routing follows ``logits`` (the
     GPU's fp32 keys) when given, else the oracle's own fp64 logits.
+
+    With std-scaled router noise (noise_scale > 0) the noise strength
+    noise_scale * std_t is taken without gradient: it sets how far the router
+    explores, it is not a path for training the router, so dz is the same as
+    for that noise added as a fixed input.
 
     Returns dict(dx, dWg, dbias, dW1, dW3, dW2, db1, db2, dgates, dz,
     shared=dict(...) or None) plus the routing dict under "route"."""
@@ -132,7 +137,8 @@ def moe_backward(inp: dict, k: int, c, act: str, dy, alpha: float = 0.0, tau: fl
     E = inp["Wg"].shape[0]
     C = F.capacity(c, k, T, E)
     if logits is None:
-        logits = F.router_logits(x, inp["Wg"], inp.get("bias"), inp.get("noise"), tau)
+        logits = F.router_logits(x, inp["Wg"], inp.get("bias"), inp.get("noise"), tau,
+                                 noise_scale)
     r = F.route_from_logits(logits, k, C)
     ids, slot_of, g = r["ids"], r["slot_of"], r["gates"]
     dyf = F.as_f64(dy)

@@ -34,6 +34,9 @@ rests on is named with it):
 * One key l = (x W_g^T + b + g) / tau drives selection, gates and P_i.
 * Capacity is the closed form of [MoE-math] 2.3, evaluated in exact rational
   arithmetic.
+* Std-scaled router noise ([MoE-math] 3.3: the noise strength follows the
+  logits' standard deviation rather than a fixed scale) uses each token's own
+  population standard deviation over its E pre-noise logits (bias included).
 * Drop priority is token order (the stable sort of [MoE-math] 3.2): a slot
   (t, j) of expert e is kept iff fewer than C earlier tokens chose e. Dropped
   slots are not re-routed and the surviving gates are not renormalised again.
@@ -83,17 +86,39 @@ def capacity(c, k: int, T: int, E: int) -> int:
 # --------------------------------------------------------------------------
 # router  ([MoE-math] 2.1, 3.2; [MoE-guide] 3.3 for bias/noise/temperature)
 # --------------------------------------------------------------------------
-def router_logits(x, Wg, bias=None, noise=None, tau: float = 1.0):
-    """l[t,i] = (sum_j x[t,j] Wg[i,j] + b_i + g[t,i]) / tau, fp64.
-    Wg is stored [E, d] (nn.Linear convention of the gate in [MoE-math] 3.2)."""
+def router_logits(x, Wg, bias=None, noise=None, tau: float = 1.0,
+                  noise_scale: float = 0.0):
+    """l[t,i] = (z[t,i] + g[t,i]) / tau with z[t,i] = sum_j x[t,j] Wg[i,j] + b_i,
+    fp64. Wg is stored [E, d] (nn.Linear convention of the gate in
+    [MoE-math] 3.2).
+
+    The noise: with noise_scale == 0 it is added as given, g = noise (a fixed
+    strength, or Gumbel noise: [MoE-guide] 3.3). With noise_scale > 0 its
+    strength follows the token's own logits, as [MoE-math] 3.3 recommends
+    over a fixed scale: g[t,i] = noise_scale * std_t * noise[t,i], where std_t
+    is the population standard deviation of z[t, :] over the E experts (the
+    logits before the noise; bias included)."""
     x = as_f64(x)
     Wg = as_f64(Wg)
     z = x @ Wg.T
     if bias is not None:
         z = z + as_f64(bias)[None, :]
     if noise is not None:
-        z = z + as_f64(noise)
+        n = as_f64(noise)
+        if noise_scale:
+            z = z + float(noise_scale) * logit_std(z)[:, None] * n
+        else:
+            z = z + n
     return z / float(tau)
+
+
+def logit_std(z):
+    """Population standard deviation of each row: sqrt(mean_i (z_i - mean z)^2).
+    Pinned: the two-expert closed form |z_0 - z_1| / 2 and the scale and
+    shift behaviour of the std-scaled router noise (tests)."""
+    z = np.asarray(z, dtype=np.float64)
+    m = z.mean(axis=1, keepdims=True)
+    return np.sqrt(((z - m) ** 2).mean(axis=1))
 
 
 def softmax(l):
@@ -291,7 +316,7 @@ def shared_expert_rows(xr, shared: dict, act: str):
 
 
 def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
-                tokens=None, logits=None, shared=None):
+                tokens=None, logits=None, shared=None, noise_scale: float = 0.0):
     """The layer: router -> softmax -> top-k -> gates -> dispatch -> experts ->
     combine -> aux statistics.
 
@@ -302,6 +327,8 @@ def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
     always computed for the whole batch, since capacity couples tokens).
     ``shared``: optional shared-expert weights (see shared_expert_rows),
     added with weight 1 to every token's output.
+    ``noise_scale``: > 0 scales the router noise by each token's logit
+    standard deviation (see router_logits).
     Returns the routing dict plus y [len(tokens) or T, d]."""
     x = inp["x"]
     T = x.shape[0]
@@ -309,7 +336,7 @@ def moe_forward(inp: dict, k: int, c, act: str, tau: float = 1.0,
     C = capacity(c, k, T, E)
     if logits is None:
         logits = router_logits(x, inp["Wg"], inp.get("bias"), inp.get("noise"),
-                               tau)
+                               tau, noise_scale)
     r = route_from_logits(logits, k, C)
     r["C"] = C
     tok = np.arange(T) if tokens is None else np.asarray(tokens)

@@ -373,6 +373,73 @@ def pin_combine_rows_is_layer_output(o):
         assert (y[dead] == 0).all()
 
 
+# ---------------------------------------------------------------- std-scaled router noise
+# kwkr.cn MoE article, section 3.3: the router noise strength follows the
+# standard deviation of the current logits instead of a fixed scale.
+def pin_std_noise_two_experts_closed_form(o):
+    """E = 2: the population std of a token's two logits is |z0 - z1| / 2, so
+    the keys are (z + s |z0 - z1| / 2 n) / tau (z from F.linear, tau != 1)."""
+    rng = _rng(21)
+    T, d, s, tau = 50, 7, 0.3, 2.0
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((2, d))
+    b = rng.standard_normal(2)
+    n = rng.standard_normal((T, 2))
+    z = F.linear(torch.from_numpy(x), torch.from_numpy(Wg), torch.from_numpy(b)).numpy()
+    half = np.abs(z[:, 0] - z[:, 1])[:, None] / 2.0
+    want = (z + s * half * n) / tau
+    got = o.router_logits(x, Wg, b, n, tau, noise_scale=s)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def pin_std_noise_follows_logit_scale(o):
+    """Scaling the tokens by a > 0 scales every key by a (bias 0, tau 1), so
+    the routing does not change: the noise grows with the logits. A fixed-scale
+    noise would not satisfy this."""
+    rng = _rng(22)
+    T, d, E, k = 64, 12, 6, 2
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, d))
+    n = rng.standard_normal((T, E))
+    base = o.router_logits(x, Wg, None, n, 1.0, noise_scale=0.5)
+    for a in (0.25, 3.0, 40.0):
+        got = o.router_logits(a * x, Wg, None, n, 1.0, noise_scale=0.5)
+        np.testing.assert_allclose(got, a * base, rtol=1e-12, atol=1e-12)
+        assert np.array_equal(o.topk_ids(got, k), o.topk_ids(base, k))
+
+
+def pin_std_noise_shift(o):
+    """A common shift c of every expert's bias leaves each token's std
+    unchanged, so every key moves by exactly c / tau."""
+    rng = _rng(23)
+    T, d, E, tau, c = 40, 9, 5, 1.5, 0.75
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E, d))
+    b = rng.standard_normal(E)
+    n = rng.standard_normal((T, E))
+    k0 = o.router_logits(x, Wg, b, n, tau, noise_scale=0.2)
+    k1 = o.router_logits(x, Wg, b + c, n, tau, noise_scale=0.2)
+    np.testing.assert_allclose(k1 - k0, c / tau, rtol=0, atol=1e-12)
+
+
+def pin_std_noise_flat_logits_get_none(o):
+    """W_g = 0, no bias: every token's logits are equal, the std is 0, so
+    the noise vanishes and every token takes experts 0..k-1 (ties to the lower
+    index) with gates 1/k; with noise_scale = 0 the same noise would be added
+    as given."""
+    rng = _rng(24)
+    T, d, E, k = 20, 5, 4, 2
+    x = rng.standard_normal((T, d))
+    n = rng.standard_normal((T, E))
+    l = o.router_logits(x, np.zeros((E, d)), None, n, 1.0, noise_scale=0.7)
+    assert (l == 0).all()
+    r = o.route_from_logits(l, k, T)
+    assert (r["ids"] == np.arange(k)[None, :]).all()
+    np.testing.assert_allclose(r["gates"], 1.0 / k, rtol=0, atol=1e-15)
+    l0 = o.router_logits(x, np.zeros((E, d)), None, n, 1.0, noise_scale=0.0)
+    np.testing.assert_allclose(l0, n, rtol=0, atol=0)
+
+
 def pin_activations_match_library(o):
     u = np.linspace(-8, 8, 1001)
     ut = torch.from_numpy(u)
@@ -520,12 +587,12 @@ def _mutants():
         return o.__dict__["_orig_ffn"](xr, W1e, W2e, W3e, b1e, None, act)
     m["ffn_drops_b2"] = ("expert_ffn_rows", ffn_no_b2)
 
-    def logits_no_bias(x, Wg, bias=None, noise=None, tau=1.0):
-        return o.__dict__["_orig_logits"](x, Wg, None, noise, tau)
+    def logits_no_bias(x, Wg, bias=None, noise=None, tau=1.0, noise_scale=0.0):
+        return o.__dict__["_orig_logits"](x, Wg, None, noise, tau, noise_scale)
     m["router_drops_bias"] = ("router_logits", logits_no_bias)
 
-    def logits_tau_mul(x, Wg, bias=None, noise=None, tau=1.0):
-        return o.__dict__["_orig_logits"](x, Wg, bias, noise, 1.0) * tau
+    def logits_tau_mul(x, Wg, bias=None, noise=None, tau=1.0, noise_scale=0.0):
+        return o.__dict__["_orig_logits"](x, Wg, bias, noise, 1.0, noise_scale) * tau
     m["router_tau_multiplies"] = ("router_logits", logits_tau_mul)
 
     def combine_no_gate(tokens, x, ids, gates, slot_of, *a, **kw):
@@ -550,6 +617,23 @@ def _mutants():
         n = np.asarray(Yrows).shape[0]
         return o.__dict__["_orig_combine_rows"](Yrows, np.where(s >= 0, (s + 1) % n, s), gates)
     m["combine_rows_wrong_row"] = ("combine_rows", combine_rows_next_row)
+
+    def std_over_tokens(z):
+        z = np.asarray(z, dtype=np.float64)
+        return np.broadcast_to(z.std(axis=0).mean(), (z.shape[0],)).copy()
+    m["noise_std_over_tokens"] = ("logit_std", std_over_tokens)
+    m["noise_std_sample_ddof1"] = ("logit_std", lambda z: np.asarray(z, float).std(axis=1, ddof=1))
+    m["noise_variance_not_std"] = ("logit_std", lambda z: np.asarray(z, float).var(axis=1))
+
+    def logits_noise_not_over_tau(x, Wg, bias=None, noise=None, tau=1.0, noise_scale=0.0):
+        l = o.__dict__["_orig_logits"](x, Wg, bias, None, tau, 0.0)
+        if noise is None:
+            return l
+        if not noise_scale:
+            return l + o.as_f64(noise) / tau
+        z = l * tau
+        return l + noise_scale * o.logit_std(z)[:, None] * o.as_f64(noise)
+    m["noise_not_divided_by_tau"] = ("router_logits", logits_noise_not_over_tau)
 
     def softmax_no_max_over_wrong_axis(l):
         e = np.exp(np.asarray(l, float))

@@ -165,6 +165,29 @@ def test_top1_gates_carry_no_router_gradient():
     assert np.all(got["dWg"] == 0.0)
 
 
+def test_std_scaled_noise_strength_carries_no_gradient():
+    """With std-scaled router noise (kwkr.cn MoE article, section 3.3) the
+    strength s * std_t is taken without gradient: the gradients equal those
+    of the same noise frozen into a fixed input, s * std_t(z) * n, with std_t
+    computed here by torch (population std of z = x W_g^T + b per token).
+    The finite-difference and autograd pins cover the fixed-input case."""
+    for act, k, tau in (("gelu", 2, 1.3), ("swiglu", 1, 1.0)):
+        inp, _, dy = _tiny(act, 9, T=20, k=k)
+        inp["noise"] = np.random.default_rng(19).standard_normal(inp["noise"].shape)
+        s = 0.4
+        got = B.moe_backward(inp, k, Fraction(3, 4), act, dy, alpha=0.1, tau=tau,
+                             noise_scale=s)
+        z = torch.nn.functional.linear(torch.from_numpy(inp["x"]), torch.from_numpy(inp["Wg"]),
+                                       torch.from_numpy(inp["bias"]))
+        frozen = (s * z.std(dim=1, unbiased=False)[:, None]).numpy() * inp["noise"]
+        ref = B.moe_backward(dict(inp, noise=frozen), k, Fraction(3, 4), act, dy, alpha=0.1,
+                             tau=tau)
+        np.testing.assert_array_equal(got["route"]["ids"], ref["route"]["ids"])
+        np.testing.assert_array_equal(got["route"]["slot_of"], ref["route"]["slot_of"])
+        for key in ("dx", "dWg", "dbias", "dW1", "dW2", "dz"):
+            np.testing.assert_allclose(got[key], ref[key], rtol=1e-10, atol=1e-12, err_msg=key)
+
+
 def test_balance_gradient_closed_form_on_a_uniform_router():
     """W_g = 0, no bias or noise, dy = 0: p = 1/E everywhere and only the
     balance term acts, dl_ti = (alpha / T) (f_i - 1/E)."""
