@@ -41,6 +41,8 @@ METRIC = ("MoE-layer fwd tokens/s at 1 B300; expert-GEMM TFLOP/s % of BF16 peak;
           "router/dispatch GB/s")
 UNIT = "tokens/s"
 L2_BYTES = 126 * 1024 * 1024
+# B300 dense bf16 tensor-core rate (no sparsity), NVIDIA's nominal figure
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def dist_env():
@@ -157,11 +159,30 @@ def algorithmic(w, kept: int, n_active: int):
     gemm_b = n_active * nm * d * H * s + 2 * kept * d * s
     comb_b = kept * d * s + T * k * 8 + T * d * s
     return dict(router_bytes=router_b, router_flops=router_f, dispatch_bytes=disp_b,
-                gemm_flops=gemm_f, gemm_bytes=gemm_b, combine_bytes=comb_b)
+                gemm_flops=gemm_f, gemm_bytes=gemm_b, combine_bytes=comb_b,
+                tc_router=w.dtype == "bf16" and E <= 64)
 
 
 def footprint_bytes(inp):
     return sum(v.numel() * v.element_size() for v in inp.values() if v is not None)
+
+
+def rotating_sets(fp: int) -> int:
+    """Input + weight sets the GPU arm rotates over: their total exceeds three
+    times the L2 cache, so no step finds the previous step's data in L2."""
+    return max(2, math.ceil(3 * L2_BYTES / fp))
+
+
+def bench_config(w, capacity: int, kept: int, n_active: int, nsets: int, fp: int,
+                 world: int) -> dict:
+    """The ``config`` object of both arms' JSON lines (the same keys and
+    values, so that the two lines describe one workload)."""
+    return dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
+                capacity=capacity, kept_rows=kept, active_experts=n_active,
+                parallelism=f"replicas x{world}",
+                launch="one CUDA graph per input set, one layer call each",
+                l2=f"{nsets} rotating input+weight sets of {fp / 2**20:.0f} MiB "
+                   f"(> L2 between reuses)")
 
 
 def time_backward(w, cfg, inp, ws, stream, dev, kept, reps):
@@ -241,10 +262,25 @@ def time_oracle(w, target_s=12.0, seed=0):
         n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3) / 2)))
         t = run(n)
     return dict(value=n / t, unit=UNIT, cores=cores, kind="oracle",
-                sample=(f"first {n} of {w.T} tokens of the seed-{w.seed} {w.name} batch as a "
-                        f"batch of their own (capacity recomputed): full fp64 numpy forward "
-                        f"(router, top-k, dispatch, experts, combine, statistics) in {t:.2f} s"),
-                seconds=t, tokens=n)
+                sample=sample_label(w, n, t), seconds=t, tokens=n)
+
+
+def sample_label(w, n: int, t: float) -> str:
+    head = "" if n == w.T else f"extrapolated ({n} of {w.T} tokens): "
+    return (f"{head}first {n} of {w.T} tokens of the seed-{w.seed} {w.name} batch as a "
+            f"batch of their own (capacity recomputed): full fp64 numpy forward "
+            f"(router, top-k, dispatch, experts, combine, statistics) in {t:.2f} s")
+
+
+def oracle_routing_summary(w, inp):
+    """Kept rows and active experts of the whole batch, from the oracle's own
+    routing (the reference arm's copy of the GPU arm's config keys)."""
+    from oracle import moe_oracle as ORC
+    T = inp["x"].shape[0]
+    C = ORC.capacity(w.c, w.k, T, w.E)
+    lg = ORC.router_logits(inp["x"], inp["Wg"], inp.get("bias"), inp.get("noise"), w.tau)
+    r = ORC.route_from_logits(lg, w.k, C)
+    return C, int(r["offset"][-1]), int((np.diff(r["offset"]) > 0).sum())
 
 
 def run_reference(args, w):
@@ -266,16 +302,76 @@ def run_reference(args, w):
         ORC.moe_forward(sub, k=w.k, c=w.c, act=w.act, tau=w.tau)
     dt = (time.perf_counter() - t0) / args.steps
     value = n / dt
+    C, kept, n_active = oracle_routing_summary(w, inp)
+    fp = footprint_bytes(inp)
+    cfg = bench_config(w, C, kept, n_active, rotating_sets(fp), fp, world)
     line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
                 warmup=args.warmup, ms_per_step=dt * 1e3, higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
                 impl="reference",
-                config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
-                            sample_tokens=n),
+                config=cfg,
                 cpu_baseline=dict(value=value, unit=UNIT, cores=per_step["cores"],
-                                  kind="oracle", sample=per_step["sample"]),
+                                  kind="oracle", sample=sample_label(w, n, dt)),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- stage times
+STAGES = ["router", "dispatch", "gemm1", "gemm2", "combine_stats"]
+
+
+def _stage_avg(evs):
+    n = len(evs)
+    st = {name: sum(r[j].elapsed_time(r[j + 1]) for r in evs) / n
+          for j, name in enumerate(STAGES)}
+    st["layer"] = sum(r[0].elapsed_time(r[5]) for r in evs) / n
+    return st
+
+
+def stage_times(moe, cfg, sets, nsets, ws, out, stream, dev, want):
+    """Per-stage device times of the layer call, averaged over about ``want``
+    calls. The calls run as replays of one CUDA graph of M consecutive
+    moe_layer_forward_profiled calls (rotating over the input sets), each with
+    its own six events, which become event nodes of the graph; so the
+    stages are timed on the same graph-launched path as the timed steps (an
+    event node between two kernels does stop the next kernel's prologue from
+    overlapping its predecessor's tail). Falls back to eager calls if the
+    capture fails."""
+    M = 8
+    reps = max(2, math.ceil(want / M))
+
+    def new_events(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
+        for row in evs:
+            for e in row:
+                e.record(stream)  # create the events
+        return evs
+
+    try:
+        evs = new_events(M)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(M):
+                moe.layer_forward_profiled(cfg, sets[i % nsets], evs[i], ws=ws, out=out)
+        g.replay()  # warm-up replay
+        torch.cuda.synchronize(dev)
+        acc = []
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize(dev)
+            acc.append(_stage_avg(evs))
+        st = {k: sum(a[k] for a in acc) / len(acc) for k in acc[0]}
+        return st, (f"CUDA-graph replays: {reps} x {M} consecutive moe_layer_forward_profiled "
+                    f"calls with event nodes at the stage boundaries")
+    except Exception as exc:  # pragma: no cover - capture not available
+        torch.cuda.synchronize(dev)
+        evs = new_events(want)
+        torch.cuda.synchronize(dev)
+        for i in range(want):
+            moe.layer_forward_profiled(cfg, sets[i % nsets], evs[i], ws=ws, out=out)
+        torch.cuda.synchronize(dev)
+        return _stage_avg(evs), f"eager moe_layer_forward_profiled calls ({exc.__class__.__name__})"
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -286,7 +382,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     # the shared-expert variant (moe_layer_forward_shared) is covered by the
     # parity tests; the bench times the routed layer
-    ap.add_argument("--workload", default="switch_top1",
+    ap.add_argument("--workload", default="mixtral",
                     choices=sorted(n for n, v in W.WORKLOADS.items() if v.shared_H == 0))
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -316,7 +412,7 @@ def main():
     # ---- inputs: rotating sets, different seed per rank and per set
     base = W.make_inputs(w, seed=rank_seed(w, rank, 0))
     fp = footprint_bytes(base)
-    nsets = max(2, math.ceil(3 * L2_BYTES / fp))
+    nsets = rotating_sets(fp)
     sets = [W.to_device(base, dev)]
     for i in range(1, nsets):
         sets.append(W.to_device(W.make_inputs(w, seed=rank_seed(w, rank, i)), dev))
@@ -355,10 +451,23 @@ def main():
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-
+    # then keep stepping, untimed, until the GPU has run the layer for about
+    # 1.5 s: the timed region starts in the clock and power state of a long
+    # run (dense layers reach the power limit within milliseconds, and its
+    # throttle reason is reported only once the limit has held for a while).
+    # The clock sampler starts first, so that the GPU does not idle between
+    # these steps and the timed ones.
     clocks = ClockSampler(local_rank) if rank == 0 else None
     if clocks:
         clocks.start()
+    t_warm = time.time() + 1.5
+    i = args.warmup
+    while time.time() < t_warm:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -389,19 +498,8 @@ def main():
 
     # ---- live stage times: the same steps through moe_layer_forward_profiled,
     # which records CUDA events on this stream at the stage boundaries
-    prof_steps = max(10, min(args.steps, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(prof_steps)]
-    for row in evs:
-        for e in row:
-            e.record(stream)  # create the events
-    torch.cuda.synchronize(dev)
-    for i in range(prof_steps):
-        moe.layer_forward_profiled(cfg, sets[i % nsets], evs[i], ws=ws, out=out)
-    torch.cuda.synchronize(dev)
-    names = ["router", "dispatch", "gemm1", "gemm2", "combine_stats"]
-    st = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(prof_steps)) / prof_steps
-          for j, n in enumerate(names)}
-    st["layer"] = sum(evs[i][0].elapsed_time(evs[i][5]) for i in range(prof_steps)) / prof_steps
+    st, stage_how = stage_times(moe, cfg, sets, nsets, ws, out, stream, dev,
+                                max(10, min(args.steps, 200)))
 
     # ---- end to end through the host-buffer C call (pinned host x and y):
     # every step copies its tokens in, runs the layer and copies y (and
@@ -456,7 +554,8 @@ def main():
                 gemm1=dict(ms=st["gemm1"], tflops=g1_flops / (st["gemm1"] / 1e3) / 1e12),
                 gemm2=dict(ms=st["gemm2"], tflops=g2_flops / (st["gemm2"] / 1e3) / 1e12),
                 frac_of_sustained=(achieved / peaks["bf16_tflops_sustained"]
-                                   if peaks.get("bf16_tflops_sustained") else None))
+                                   if peaks.get("bf16_tflops_sustained") else None),
+                frac_of_nominal_dense=achieved / NOMINAL_BF16_TFLOPS)
 
     # ---- backward pass of the same layer call (moe_layer_backward), timed
     # alone with CUDA events after one forward call that left its state in ws
@@ -471,18 +570,14 @@ def main():
 
     if rank == 0:
         hbm = peaks["hbm_gbs"]
+        comb_ms = st["combine_stats"] if w.k > 1 or not work["tc_router"] else None
         line = dict(
             metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
             warmup=args.warmup, ms_per_step=ms, eager_ms_per_step=eager_ms,
             higher_is_better=True, scaling="weak",
             vs_baseline=None, dtype="bf16" if w.dtype == "bf16" else "f32",
             data="synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
-            config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, H=w.H, act=w.act,
-                        capacity=cfg.capacity, kept_rows=kept, active_experts=n_active,
-                        parallelism=f"replicas x{world}",
-                        launch="one CUDA graph per input set, one layer call each",
-                        l2=f"{nsets} rotating input+weight sets of {fp / 2**20:.0f} MiB "
-                           f"(> L2 between reuses)"),
+            config=bench_config(w, cfg.capacity, kept, n_active, nsets, fp, world),
             roofline=roof,
             cpu_baseline=cpu,
             e2e=dict(value=w.T * world / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=bytes_x,
@@ -495,12 +590,23 @@ def main():
             stages_roofline=dict(
                 router_gbs=work["router_bytes"] / (st["router"] / 1e3) / 1e9,
                 router_hbm_frac=work["router_bytes"] / (st["router"] / 1e3) / 1e9 / hbm,
+                dispatch_gbs=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9,
+                dispatch_hbm_frac=work["dispatch_bytes"] / (st["dispatch"] / 1e3) / 1e9 / hbm,
+                combine_gbs=(None if comb_ms is None
+                             else work["combine_bytes"] / (comb_ms / 1e3) / 1e9),
+                combine_hbm_frac=(None if comb_ms is None
+                                  else work["combine_bytes"] / (comb_ms / 1e3) / 1e9 / hbm),
                 gemm_tflops=achieved, gemm_frac_burst=achieved / peak,
+                gemm_frac_nominal_dense=achieved / NOMINAL_BF16_TFLOPS,
                 gemm_weight_gbs=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9,
                 gemm_weight_hbm_frac=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9 / hbm,
                 hbm_peak_gbs=hbm,
-                note="stage times from moe_layer_forward_profiled events; for k = 1 the "
-                     "combine runs inside GEMM2"),
+                bytes=dict(router=work["router_bytes"], dispatch=work["dispatch_bytes"],
+                           combine=work["combine_bytes"], gemm=work["gemm_bytes"]),
+                note=(f"stage times from {stage_how}; dispatch = per-tile dispatch + gather "
+                      f"launches; " + ("for k = 1 the combine runs inside GEMM2 (no combine "
+                                       "stage)" if comb_ms is None else
+                                       "combine = the combine launch"))),
             device_status=status[0],
             backward=bwd,
         )

@@ -78,13 +78,22 @@ typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
 
 /* Layer shape. capacity is C (see moe_capacity). tau is the router
  * temperature (logits are divided by it; 1.0 = none). dtype and act hold a
- * moe_dtype_t and a moe_act_t. */
+ * moe_dtype_t and a moe_act_t.
+ * noise_scale sets how the router noise input (where one is passed) enters
+ * the logits: 0 adds it as given (a fixed-strength noise, or Gumbel noise:
+ * the lpnh.cn MoE guide, section 3.3); s > 0 scales it by s times the
+ * token's standard deviation over its E logits before the noise (bias
+ * included; population form), so that the noise strength follows the
+ * logits' scale (the kwkr.cn MoE article, section 3.3):
+ *   l[t,i] = (z[t,i] + s * std_t(z) * noise[t,i]) / tau.
+ * Must be finite and >= 0. */
 typedef struct {
   int32_t T, d, E, k, H;
   int32_t capacity;
   int32_t dtype;
   int32_t act;
   float tau;
+  float noise_scale;
 } moe_config_t;
 
 /* Version of this ABI (major * 100 + minor). */
@@ -265,7 +274,9 @@ MOE_API moe_status_t moe_layer_forward_shared(const moe_config_t *cfg,
  * dispatch, after GEMM1 (the hidden activation), after GEMM2 and after the
  * combine and statistics. Where a path has no boundary between two marks
  * (the fp32 path runs both GEMMs in one call) both are recorded at the same
- * point. Results are identical to moe_layer_forward. */
+ * point. Results are identical to moe_layer_forward. Called while `stream`
+ * is being captured into a CUDA graph, the marks become event-record nodes
+ * of the graph (cudaEventRecordExternal), recorded at every replay. */
 MOE_API moe_status_t moe_layer_forward_profiled(const moe_config_t *cfg,
                                                 const moe_layer_inputs_t *in,
                                                 const moe_layer_outputs_t *out, void *ws,
@@ -306,13 +317,46 @@ MOE_API moe_status_t moe_workspace_size_backward(const moe_config_t *cfg, size_t
  * dtype); alpha the weight of L_balance. The expert pre-activations are
  * recomputed (for the activation's derivative). Every sum is taken in
  * a fixed order (results are run-to-run identical). Covered: bf16 with
- * E <= 64 (the tensor-core forward); no shared expert. Nothing is enqueued
- * on a validation failure. */
+ * E <= 64 (the tensor-core forward); a layer with a shared expert uses
+ * moe_layer_backward_shared. Nothing is enqueued on a validation failure. */
 MOE_API moe_status_t moe_layer_backward(const moe_config_t *cfg, const moe_layer_inputs_t *in,
                                         const moe_layer_outputs_t *fwd, const void *dy,
                                         float alpha, const moe_layer_grads_t *grads,
                                         const void *ws, size_t ws_bytes, void *bwd_ws,
                                         size_t bwd_ws_bytes, moe_stream_t stream);
+
+/* Gradients of the shared expert's weights (fp32), the layout of the
+ * moe_shared_expert_t weights. */
+typedef struct {
+  float *dW1;     /* [Hs, d] required                                      */
+  float *dW3;     /* [Hs, d] SwiGLU (required), else NULL                  */
+  float *dW2;     /* [d, Hs] required                                      */
+  float *db1;     /* [Hs] GELU: required iff shared->b1, else NULL         */
+  float *db2;     /* [d]  GELU: required iff shared->b2, else NULL         */
+} moe_shared_grads_t;
+
+/* Bytes of the backward workspace of a layer with a shared expert of hidden
+ * size H_shared (a multiple of 8). Host only. */
+MOE_API moe_status_t moe_workspace_size_backward_shared(const moe_config_t *cfg,
+                                                        int32_t H_shared, size_t *bytes);
+
+/* Backward of one moe_layer_forward_shared call (the shared expert of the
+ * lpnh.cn MoE guide, section 4.10: an always-on expert added with weight 1 to
+ * every token's output). As moe_layer_backward, with the same shared expert
+ * and the forward's workspace ws (moe_workspace_size_shared bytes; it holds
+ * the shared expert's hidden activations); bwd_ws holds
+ * moe_workspace_size_backward_shared bytes. The shared expert's output
+ * gradient is dy itself: its weight gradients go to shared_grads and its
+ * input gradient is added into grads->dx in the same fixed-order sum as the
+ * routed and router terms. */
+MOE_API moe_status_t moe_layer_backward_shared(const moe_config_t *cfg,
+                                               const moe_layer_inputs_t *in,
+                                               const moe_shared_expert_t *shared,
+                                               const moe_layer_outputs_t *fwd, const void *dy,
+                                               float alpha, const moe_layer_grads_t *grads,
+                                               const moe_shared_grads_t *shared_grads,
+                                               const void *ws, size_t ws_bytes, void *bwd_ws,
+                                               size_t bwd_ws_bytes, moe_stream_t stream);
 
 /* Number of kernels one moe_layer_forward call launches for this shape
  * (0 if cfg is invalid). Host only. */

@@ -30,19 +30,39 @@ def nvcc_path() -> str:
 
 
 def build(verbose: bool = False, extra: list[str] | None = None) -> str:
+    """Compile every source to an object file (in parallel, one nvcc per
+    file, objects under _build/ beside the sources) and link the shared
+    library."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
-    cmd = [nvcc_path(), "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-lineinfo", *ARCH, "-cudart", "static", "-Xcompiler", "-fvisibility=hidden",
-           "-DMOE_BUILD_SO", "-I", os.path.join(HERE, "..", "include"),
-           *(extra or []), "-o", LIB + ".tmp", *srcs]
-    if verbose:
-        print(" ".join(cmd))
+    objdir = os.path.join(HERE, "_build")
+    os.makedirs(objdir, exist_ok=True)
+    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo", *ARCH,
+              "-Xcompiler", "-fvisibility=hidden", "-DMOE_BUILD_SO",
+              "-I", os.path.join(HERE, "..", "include"), *(extra or [])]
+    objs, procs = [], []
+    for src in srcs:
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        objs.append(obj)
+        cmd = [nvcc_path(), *common, "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd))
+        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                            stderr=subprocess.STDOUT, text=True)))
+    failed = False
+    for src, pr in procs:
+        out, _ = pr.communicate()
+        if pr.returncode != 0:
+            sys.stderr.write(out)
+            failed = True
+        elif verbose and out:
+            print(out)
+    if failed:
+        raise RuntimeError("nvcc failed building libmoe_b300.so")
+    cmd = [nvcc_path(), "-shared", *ARCH, "-cudart", "static", "-o", LIB + ".tmp", *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed building libmoe_b300.so")
-    if verbose and (r.stdout or r.stderr):
-        print(r.stdout + r.stderr)
+        raise RuntimeError("nvcc failed linking libmoe_b300.so")
     os.replace(LIB + ".tmp", LIB)
     return LIB
 

@@ -110,6 +110,7 @@ moe_status_t validate(const moe_config_t* c) {
   const int align = c->dtype == MOE_F32 ? 4 : 8;
   if (c->d % align || c->H % align) return MOE_ERR_INVALID_ARG;
   if (!(c->tau > 0.f) || !isfinite(c->tau)) return MOE_ERR_INVALID_ARG;
+  if (!(c->noise_scale >= 0.f) || !isfinite(c->noise_scale)) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxE || c->k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->d >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED;
@@ -133,7 +134,7 @@ template <typename T> T* at(void* ws, size_t off) {
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 100; }
+int32_t moe_abi_version(void) { return 101; }
 
 const char* moe_status_string(int32_t status) {
   switch (status) {
@@ -273,7 +274,7 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
                                        void* ws, cudaStream_t s,
                                        const cudaEvent_t* ev = nullptr,
                                        const moe_shared_expert_t* sh = nullptr) {
-  auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+  auto mark = [&](int i) -> cudaError_t { return ev ? record_stage_event(ev[i], s) : cudaSuccess; };
   const moe_config_t& c = *cfg;
   const WsLayout L = ws_layout(c, 0, sh ? sh->H : 0);
   int32_t* idx = out && out->topk_idx ? out->topk_idx : at<int32_t>(ws, L.topk_idx);
@@ -497,6 +498,40 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   return L;
 }
 bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && router_tc_supported(c); }
+
+// The shared expert's part of the backward workspace, after the routed part:
+// its recomputed pre-activations and activation gradients [T, Hps], its dx
+// term [T, d], the transposed [W1^T | W3^T] where needed, one-group offsets.
+struct BwdSharedLayout {
+  size_t pre, dact, dxs, W13T, soff, total;
+};
+moe_config_t shared_config(const moe_config_t& c, int H_shared) {
+  moe_config_t cs = c;
+  cs.E = 1;
+  cs.k = 1;
+  cs.H = H_shared;
+  cs.capacity = c.T;
+  return cs;
+}
+BwdSharedLayout bwd_shared_layout(const moe_config_t& c, int H_shared) {
+  BwdSharedLayout L;
+  const moe_config_t cs = shared_config(c, H_shared);
+  const size_t T = (size_t)c.T, d = (size_t)c.d;
+  const size_t Hps = c.act == MOE_ACT_SWIGLU ? 2 * (size_t)H_shared : (size_t)H_shared;
+  size_t off = bwd_layout(c).total;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return at;
+  };
+  L.pre = take(T * Hps * 2);
+  L.dact = take(T * Hps * 2);
+  L.dxs = take(T * d * 2);
+  L.W13T = take(bwd_w13_transposed(cs) ? d * Hps * 2 : 0);
+  L.soff = take(8);
+  L.total = off;
+  return L;
+}
 }  // namespace
 
 moe_status_t moe_workspace_size_backward(const moe_config_t* cfg, size_t* bytes) {
@@ -508,10 +543,13 @@ moe_status_t moe_workspace_size_backward(const moe_config_t* cfg, size_t* bytes)
   return MOE_OK;
 }
 
-moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_t* in,
-                                const moe_layer_outputs_t* fwd, const void* dy, float alpha,
-                                const moe_layer_grads_t* g, const void* ws, size_t ws_bytes,
-                                void* bws, size_t bws_bytes, moe_stream_t stream) {
+static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                        const moe_shared_expert_t* sh,
+                                        const moe_layer_outputs_t* fwd, const void* dy,
+                                        float alpha, const moe_layer_grads_t* g,
+                                        const moe_shared_grads_t* sg, const void* ws,
+                                        size_t ws_bytes, void* bws, size_t bws_bytes,
+                                        moe_stream_t stream) {
   moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
   const moe_config_t& c = *cfg;
@@ -527,10 +565,21 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
       ((in->b1 != nullptr) != (g->db1 != nullptr)) ||
       ((in->b2 != nullptr) != (g->db2 != nullptr)))
     return MOE_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(c, 0);
-  if ((st = check_ws(const_cast<void*>(ws), ws_bytes, L.total_layer)) != MOE_OK) return st;
+  if (sh) {
+    if ((st = check_shared(cfg, sh)) != MOE_OK) return st;
+    if (!sg || !sg->dW1 || !sg->dW2 || (swiglu != (sg->dW3 != nullptr)) ||
+        ((sh->b1 != nullptr) != (sg->db1 != nullptr)) ||
+        ((sh->b2 != nullptr) != (sg->db2 != nullptr)))
+      return MOE_ERR_INVALID_ARG;
+  }
+  const int Hs = sh ? sh->H : 0;
+  const WsLayout L = ws_layout(c, 0, Hs);
+  if ((st = check_ws(const_cast<void*>(ws), ws_bytes, sh ? L.total_shared : L.total_layer)) !=
+      MOE_OK)
+    return st;
   const BwdLayout B = bwd_layout(c);
-  if ((st = check_ws(bws, bws_bytes, B.total)) != MOE_OK) return st;
+  const BwdSharedLayout BS = bwd_shared_layout(c, Hs > 0 ? Hs : 8);
+  if ((st = check_ws(bws, bws_bytes, sh ? BS.total : B.total)) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t R = max_rows(c);
   const int Hp = swiglu ? 2 * c.H : c.H;
@@ -565,7 +614,36 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   if (e == cudaSuccess)
     e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, in->W2, W13T, dYb, pre, dact, dxd,
                           R, hdr, s);
-  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s);
+  // the shared expert: the same expert backward as one group of all T token
+  // rows, its output gradient being dy itself (weight 1 for every token)
+  void* dxs = nullptr;
+  if (sh && e == cudaSuccess) {
+    const moe_config_t cs = shared_config(c, Hs);
+    const int Hps = swiglu ? 2 * Hs : Hs;
+    int32_t* soff = at<int32_t>(bws, BS.soff);
+    void* W13Ts = bwd_w13_transposed(cs) ? at<void>(bws, BS.W13T) : nullptr;
+    void* pre_s = at<void>(bws, BS.pre);
+    void* dact_s = at<void>(bws, BS.dact);
+    dxs = at<void>(bws, BS.dxs);
+    e = launch_one_group_offsets(soff, c.T, s);
+    if (e == cudaSuccess && W13Ts) {
+      e = launch_weight_transpose(sh->W1, 1, Hs, c.d, Hps, 0, W13Ts, s);
+      if (e == cudaSuccess) e = launch_weight_transpose(sh->W3, 1, Hs, c.d, Hps, Hs, W13Ts, s);
+    }
+    if (e == cudaSuccess)
+      e = launch_ffn_bwd_tc(cs, in->x, soff, sh->W1, sh->W3, sh->b1, sh->W2, W13Ts, dy, pre_s,
+                            dact_s, dxs, c.T, hdr, s);
+    // dW2s [d, Hs] = dy^T h_s (h_s as the forward left it); [dW1s; dW3s] = dact_s^T x
+    if (e == cudaSuccess)
+      e = launch_wgrad_tc(dy, c.d, at<void>(wsm, L.sh_h), Hs, c.T, soff, 1, c.d, Hs, c.d,
+                          sg->dW2, sg->dW2, hdr, s);
+    if (e == cudaSuccess)
+      e = launch_wgrad_tc(dact_s, Hps, in->x, c.d, c.T, soff, 1, Hps, c.d, Hs, sg->dW1,
+                          swiglu ? sg->dW3 : sg->dW1, hdr, s);
+    if (e == cudaSuccess && sg->db1) e = launch_expert_colsum(dact_s, Hps, Hs, soff, 1, sg->db1, s);
+    if (e == cudaSuccess && sg->db2) e = launch_expert_colsum(dy, c.d, c.d, soff, 1, sg->db2, s);
+  }
+  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s, dxs);
   if (e == cudaSuccess)
     e = launch_bwd_wg(c, dz, dzb, B.kp, in->x, at<int32_t>(bws, B.wgoff),
                       at<float>(bws, B.wg_part), g->dWg, g->dbias, hdr, s);
@@ -580,6 +658,36 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_
   if (e == cudaSuccess && g->db1) e = launch_expert_colsum(dact, Hp, c.H, off, c.E, g->db1, s);
   if (e == cudaSuccess && g->db2) e = launch_expert_colsum(dYb, c.d, c.d, off, c.E, g->db2, s);
   return cuda_status(e);
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                const moe_layer_outputs_t* fwd, const void* dy, float alpha,
+                                const moe_layer_grads_t* g, const void* ws, size_t ws_bytes,
+                                void* bws, size_t bws_bytes, moe_stream_t stream) {
+  return layer_backward_impl(cfg, in, nullptr, fwd, dy, alpha, g, nullptr, ws, ws_bytes, bws,
+                             bws_bytes, stream);
+}
+
+moe_status_t moe_workspace_size_backward_shared(const moe_config_t* cfg, int32_t H_shared,
+                                                size_t* bytes) {
+  const moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if (!bytes || H_shared < 1 || H_shared % 8) return MOE_ERR_INVALID_ARG;
+  if (!bwd_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
+  *bytes = bwd_shared_layout(*cfg, H_shared).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_backward_shared(const moe_config_t* cfg, const moe_layer_inputs_t* in,
+                                       const moe_shared_expert_t* shared,
+                                       const moe_layer_outputs_t* fwd, const void* dy,
+                                       float alpha, const moe_layer_grads_t* grads,
+                                       const moe_shared_grads_t* shared_grads, const void* ws,
+                                       size_t ws_bytes, void* bws, size_t bws_bytes,
+                                       moe_stream_t stream) {
+  if (!shared) return MOE_ERR_INVALID_ARG;
+  return layer_backward_impl(cfg, in, shared, fwd, dy, alpha, grads, shared_grads, ws, ws_bytes,
+                             bws, bws_bytes, stream);
 }
 
 }  // extern "C"

@@ -151,13 +151,15 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
 }
 
 // dx_t = sum over the kept slots of dxd[slot] (slot order) + dxr_t (the
-// router term dz_t W_g from the tensor cores), fp32, rounded once. Warp w of
-// block (bx, by) owns token bx * NW + w and a chunk of 128 16-byte vectors.
+// router term dz_t W_g from the tensor cores) [+ dxs_t, the shared expert's
+// term, if given], fp32, rounded once. Warp w of block (bx, by) owns token
+// bx * NW + w and a chunk of 128 16-byte vectors.
 constexpr int DX_UNR = 4, DX_CHUNK = 32 * DX_UNR;
 __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dxd,
                                                     const int32_t* __restrict__ slot_of,
                                                     const uint4* __restrict__ dxr, int T, int k,
-                                                    int nvec, uint4* __restrict__ dx) {
+                                                    int nvec, uint4* __restrict__ dx,
+                                                    const uint4* __restrict__ dxs) {
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T) return;
   const int lane = threadIdx.x & 31;
@@ -192,6 +194,11 @@ __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dx
     unpack8(__ldg(dxr + (size_t)t * nvec + v), a);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
+    if (dxs) {
+      unpack8(__ldg(dxs + (size_t)t * nvec + v), a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
+    }
     dx[(size_t)t * nvec + v] = pack8(acc[u]);
   }
 }
@@ -332,12 +339,12 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
 }
 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const void* dxr, void* dx, cudaStream_t s) {
+                          const void* dxr, void* dx, cudaStream_t s, const void* dxs) {
   const int nvec = c.d / 8;
   const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + DX_CHUNK - 1) / DX_CHUNK));
   bwd_dx_kernel<<<grid, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of,
                                     static_cast<const uint4*>(dxr), c.T, c.k, nvec,
-                                    static_cast<uint4*>(dx));
+                                    static_cast<uint4*>(dx), static_cast<const uint4*>(dxs));
   return cudaGetLastError();
 }
 

@@ -46,54 +46,76 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
 // base (optional, [T, d]): each token's sum starts from its base row (the
 // shared expert's output) instead of zero.
 // Warp w of block (bx, by) owns token bx * NW + w and the row chunk by of
-// CHUNK 16-byte vectors (32 lanes x UNR vectors each): a row is split over
-// several warps so that a small batch still fills the GPU, and each lane
-// issues the UNR x k loads of its vectors before it sums them.
-constexpr int UNR = 4, CHUNK = 32 * UNR;
-template <typename T>
+// 32 UNR 16-byte vectors (32 lanes x UNR vectors each): a row is split over
+// several warps so that a small batch still fills the GPU. Each lane issues
+// all of its loads (UNR vectors of each of the k slots) before it sums them:
+// a dropped slot loads the vectors of the token's first kept slot (the same
+// lines, so they come from the cache) and adds nothing, which keeps every
+// load unconditional and in flight together. A token without a kept slot
+// writes its base row, or zeros.
+template <int KM>
+struct CombineShape {
+  static constexpr int UNR = KM <= 2 ? 4 : (KM <= 4 ? 2 : 1);
+  static constexpr int CHUNK = 32 * UNR;
+};
+template <typename T, int KM>
 __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y,
                                                      const int32_t* __restrict__ slot_of,
                                                      const float* __restrict__ gate, int T_,
                                                      int k, int nvec, uint4* __restrict__ y,
                                                      const uint4* __restrict__ base) {
   constexpr int V = 16 / sizeof(T);
+  constexpr int UNR = CombineShape<KM>::UNR;
   pdl_wait();
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T_) return;
   const int lane = threadIdx.x & 31;
-  int sl[kMaxK];
-  float g[kMaxK];
+  int sl[KM];
+  float g[KM];
+  int first = -1;
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
+  for (int j = 0; j < KM; ++j) {
     sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
     g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
+    if (first < 0 && sl[j] >= 0) first = sl[j];
   }
-  const int v0 = blockIdx.y * CHUNK + lane;
+  const int v0 = blockIdx.y * CombineShape<KM>::CHUNK + lane;
   float acc[UNR][8];
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-    const int v = v0 + 32 * u;
-    if (base && v < nvec) unpack(__ldg(base + (size_t)t * nvec + v), acc[u], (T*)nullptr);
   }
-  // slot order j = 0..k-1 for every vector: the same fp32 sum order as one
-  // warp walking the row
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (sl[j] < 0) continue;
-    uint4 q[UNR];
+  if (base) {
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int v = v0 + 32 * u;
-      q[u] = v < nvec ? __ldg(Y + (size_t)sl[j] * nvec + v) : make_uint4(0, 0, 0, 0);
+      if (v < nvec) unpack(__ldg(base + (size_t)t * nvec + v), acc[u], (T*)nullptr);
     }
+  }
+  if (first >= 0) {  // the same for the whole warp (one token)
+    uint4 q[KM][UNR];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      float f[8];
-      unpack(q[u], f, (T*)nullptr);
+    for (int j = 0; j < KM; ++j) {
+      const size_t row = (size_t)(sl[j] >= 0 ? sl[j] : first);
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[u][i] = fmaf(g[j], f[i], acc[u][i]);
+      for (int u = 0; u < UNR; ++u) {
+        const int v = v0 + 32 * u;
+        q[j][u] = (j < k && v < nvec) ? __ldg(Y + row * nvec + v) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // slot order j = 0..k-1 for every vector: the same fp32 sum order as one
+    // warp walking the row
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (sl[j] < 0) continue;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        float f[8];
+        unpack(q[j][u], f, (T*)nullptr);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[u][i] = fmaf(g[j], f[i], acc[u][i]);
+      }
     }
   }
 #pragma unroll
@@ -150,18 +172,27 @@ __global__ void __launch_bounds__(NT) aux_kernel(const int32_t* __restrict__ cou
 
 }  // namespace
 
+template <int KM>
+cudaError_t launch_combine_km(const moe_config_t& c, const uint4* Y, const int32_t* slot_of,
+                              const float* gate, uint4* y, const uint4* b, cudaStream_t s) {
+  const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
+  constexpr int CHUNK = CombineShape<KM>::CHUNK;
+  const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CHUNK - 1) / CHUNK));
+  if (c.dtype == MOE_F32)
+    return launch_pdl(combine_kernel<float, KM>, grid, dim3(NT), 0, s, Y, slot_of, gate, c.T,
+                      c.k, nvec, y, b);
+  return launch_pdl(combine_kernel<__nv_bfloat16, KM>, grid, dim3(NT), 0, s, Y, slot_of, gate,
+                    c.T, c.k, nvec, y, b);
+}
+
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
                            const float* gate, void* y, cudaStream_t s, const void* base) {
-  const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
-  const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CHUNK - 1) / CHUNK));
   const uint4* b = static_cast<const uint4*>(base);
   const uint4* Yv = static_cast<const uint4*>(Y);
   uint4* yv = static_cast<uint4*>(y);
-  if (c.dtype == MOE_F32)
-    return launch_pdl(combine_kernel<float>, grid, dim3(NT), 0, s, Yv, slot_of, gate, c.T, c.k,
-                      nvec, yv, b);
-  return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(NT), 0, s, Yv, slot_of, gate, c.T,
-                    c.k, nvec, yv, b);
+  if (c.k <= 2) return launch_combine_km<2>(c, Yv, slot_of, gate, yv, b, s);
+  if (c.k <= 4) return launch_combine_km<4>(c, Yv, slot_of, gate, yv, b, s);
+  return launch_combine_km<kMaxK>(c, Yv, slot_of, gate, yv, b, s);
 }
 
 // off[0] = 0, off[1] = rows: the one-group offsets of the shared expert.

@@ -22,10 +22,11 @@ constexpr int kMaxDevices = 64;
 // uses it and held until the process exits.
 __device__ __align__(256) int32_t g_dispatch_scratch[2 * kStaticScratchEntries];
 
+// The array's device address on each device, once a lookup has succeeded
+// (a failed lookup is not kept: the next call tries again).
 struct DeviceScratch {
-  std::once_flag once;
+  std::mutex mu;
   int32_t* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
 };
 DeviceScratch g_scratch[kMaxDevices];
 
@@ -51,15 +52,25 @@ extern "C" moe_status_t moe_dispatch_static_scratch(const moe_config_t* cfg,
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
   DeviceScratch& ds = g_scratch[dev];
   // First call on this device (with it current): host code cannot use the
-  // array's name as a device address, so look the address up once.
-  std::call_once(ds.once, [&ds] {
-    ds.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&ds.ptr), g_dispatch_scratch);
-  });
-  if (ds.err != cudaSuccess || ds.ptr == nullptr) return MOE_ERR_CUDA;
+  // array's name as a device address, so look the address up; it is kept
+  // only once a lookup has succeeded.
+  int32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(ds.mu);
+    if (ds.ptr == nullptr) {
+      int32_t* p = nullptr;
+      if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_dispatch_scratch) == cudaSuccess)
+        ds.ptr = p;
+      else
+        (void)cudaGetLastError();  // do not leave the failure for a later launch check
+    }
+    scratch = ds.ptr;
+  }
+  if (scratch == nullptr) return MOE_ERR_CUDA;
   // Both arrays are fully rewritten by every call (histograms by the count
   // kernel, bases by the scan kernel), so nothing needs clearing first.
   const cudaError_t e = launch_dispatch(*cfg, topk_idx, x, expert_count, expert_offset, slot_of,
-                                        token_of_row, xd, ds.ptr, ds.ptr + kStaticScratchEntries,
+                                        token_of_row, xd, scratch, scratch + kStaticScratchEntries,
                                         (int64_t)cfg->T * cfg->k, (cudaStream_t)stream);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -1,5 +1,5 @@
 // Dispatch and load-balance statistics fed by the tensor-core router, in one
-// kernel with one block per 128-token tile.
+// kernel with one block per router tile (at most 128 tokens, a multiple of 8).
 //
 // The router already counted, for every tile, how many of the tile's slots
 // chose each expert, and summed p per expert per CTA. From those each block
@@ -16,8 +16,6 @@
 namespace moe {
 namespace {
 
-constexpr int TILE = kRouterTcTile;  // tokens per tile (128)
-
 __device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -33,20 +31,23 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-// One block of 256 threads per 128-token tile.
-//  1. tot[e] = slots of e in all tiles, base[e] = slots of e in earlier tiles
-//     (thread j sums expert j % E over every G-th tile, G = 256 / E, with
-//     coalesced reads of the router's [tiles, E] counts; then the G partials
-//     of each expert are added);
+// One block of 256 threads per router tile of `rows` tokens.
+//  1. tot[e] = slots of e in all tiles, base[e] = slots of e in earlier tiles:
+//     the router's [tiles, E] counts are read as C = E/V columns of V-int
+//     vectors (V = 4 if E is a multiple of 4, else 1); thread (g, col) sums
+//     column col over every G-th tile (G = 256 / C), sixteen independent loads
+//     per round; then R threads per expert add the G partials of the expert
+//     and combine theirs with shuffles (integer sums, so the order is
+//     immaterial);
 //  2. offset_e = sum_{e'<e} min(tot_e', C);
 //  3. block 0 writes counts, offsets and the statistics;
-//  4. stable positions: warp w owns tokens [16w, 16w + 16) of the tile (16k
-//     consecutive slots), counts them per expert, and walks them 32 at a time
-//     in token order; slot (t, j) is kept iff its position < C.
+//  4. stable positions: warp w owns tokens [w rows/8, (w+1) rows/8) of the
+//     tile (rows/8 k consecutive slots), counts them per expert, and walks them
+//     32 at a time in token order; slot (t, j) is kept iff its position < C.
 // With zero_y (k = 1 only) the y row of every token whose slot was dropped is
 // cleared, because GEMM2 then writes y only for kept tokens.
 __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
-    const int32_t* __restrict__ idx, int T, int k, int E, int C,
+    const int32_t* __restrict__ idx, int T, int k, int E, int C, int rows,
     const int32_t* __restrict__ tile_hist, int ntiles, const float* __restrict__ partial,
     int nparts, int32_t* __restrict__ count, int32_t* __restrict__ offset,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row,
@@ -61,44 +62,74 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
   for (int i = tid; i < 8 * kMaxE; i += 256) (&wcnt[0][0])[i] = 0;
   pdl_wait();
   {
-    // partial sums per (group g, expert e) into wcnt (as [2][G][E] ints),
-    // then tot/base per expert; integer sums, so the order is immaterial
-    const int G = 256 / E;  // E <= 256
+    // partial sums per (group g, expert e) into wcnt, as [2][G][E] ints
+    // (G E <= 1024), then tot/base per expert
+    const int V = (E & 3) == 0 ? 4 : 1;
+    const int ncol = E / V;
+    const int G = 256 / ncol;
     int* ptot = &wcnt[0][0];
-    int* pbase = ptot + 256;
-    if (tid < G * E) {
-      const int e = tid % E, g = tid / E;
-      int st = 0, sb = 0;
-      // eight independent loads in flight per round (at E = 64 a thread
-      // reads every 4th of 256 tiles)
-      for (int tt0 = g; tt0 < ntiles; tt0 += 8 * G) {
-        int v[8];
+    int* pbase = ptot + 1024;
+    if (tid < G * ncol) {
+      const int col = tid % ncol, g = tid / ncol;
+      int st[4] = {0, 0, 0, 0}, sb[4] = {0, 0, 0, 0};
+      for (int tt0 = g; tt0 < ntiles; tt0 += 16 * G) {
+        int4 v[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const int tt = tt0 + i * G;
-          v[i] = tt < ntiles ? tile_hist[(size_t)tt * E + e] : 0;
+          v[i] = make_int4(0, 0, 0, 0);
+          if (tt < ntiles) {
+            if (V == 4)
+              v[i] = __ldg(reinterpret_cast<const int4*>(tile_hist + (size_t)tt * E) + col);
+            else
+              v[i].x = __ldg(tile_hist + (size_t)tt * E + col);
+          }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          st += v[i];
-          if (tt0 + i * G < tile) sb += v[i];
+        for (int i = 0; i < 16; ++i) {
+          const bool before = tt0 + i * G < tile;
+          st[0] += v[i].x;
+          st[1] += v[i].y;
+          st[2] += v[i].z;
+          st[3] += v[i].w;
+          if (before) {
+            sb[0] += v[i].x;
+            sb[1] += v[i].y;
+            sb[2] += v[i].z;
+            sb[3] += v[i].w;
+          }
         }
       }
-      ptot[g * E + e] = st;
-      pbase[g * E + e] = sb;
-    }
-    __syncthreads();
-    if (tid < E) {
-      int st = 0, sb = 0;
-      for (int g = 0; g < G; ++g) {
-        st += ptot[g * E + tid];
-        sb += pbase[g * E + tid];
+      for (int i = 0; i < V; ++i) {
+        ptot[g * E + col * V + i] = st[i];
+        pbase[g * E + col * V + i] = sb[i];
       }
-      tot[tid] = st;
-      base[tid] = sb;
     }
     __syncthreads();
-    for (int i = tid; i < 2 * 256; i += 256) (&wcnt[0][0])[i] = 0;
+    // R threads per expert (R a power of two, R E <= 256, R <= 32: the R
+    // threads of an expert are neighbouring lanes of one warp)
+    int R = 32;
+    while (R * E > 256) R >>= 1;
+    {
+      const int e = tid / R, sub = tid % R;
+      int st = 0, sb = 0;
+      if (e < E) {
+        for (int g = sub; g < G; g += R) {
+          st += ptot[g * E + e];
+          sb += pbase[g * E + e];
+        }
+      }
+      for (int o = 1; o < R; o <<= 1) {
+        st += __shfl_xor_sync(0xffffffffu, st, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+      }
+      if (e < E && sub == 0) {
+        tot[e] = st;
+        base[e] = sb;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < 2 * 1024; i += 256) (&wcnt[0][0])[i] = 0;
   }
   __syncthreads();
   if (w == 0) {
@@ -147,8 +178,9 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
   }
   // ---- stable positions within the tile
   const int64_t nslots = (int64_t)T * k;
-  const int64_t s0 = ((int64_t)tile * TILE + 16 * w) * k;  // first slot of this warp
-  const int per_warp = 16 * k;
+  const int wrows = rows / 8;                                   // tokens per warp
+  const int64_t s0 = ((int64_t)tile * rows + (int64_t)wrows * w) * k;  // first slot of this warp
+  const int per_warp = wrows * k;
   for (int c = 0; c < per_warp; c += 32) {
     const int64_t s = s0 + c + lane;
     const bool in = (c + lane < per_warp) && s < nslots;
@@ -211,7 +243,8 @@ cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* id
   const int ntiles = router_tc_tiles(c);
   const int y_vec16 = (int)((size_t)c.d * elem_bytes(c) / 16);
   return launch_pdl(dispatch_tiles_kernel, dim3(ntiles), dim3(256), 0, s, idx, c.T, c.k, c.E,
-                    c.capacity, tile_hist, ntiles, partial, nparts, count, offset, slot_of,
+                    c.capacity, router_tc_rows(c), tile_hist, ntiles, partial, nparts, count,
+                    offset, slot_of,
                     token_of_row, prob_sum, f, P, Lb, dropped,
                     c.k == 1 ? static_cast<uint4*>(zero_y) : (uint4*)nullptr, y_vec16);
 }

@@ -36,6 +36,7 @@
 
 #include <math.h>
 #include <mutex>
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -46,8 +47,6 @@ constexpr int BM = 128;
 constexpr int BK = 64;       // one 128-byte swizzle row of bf16
 constexpr int UMMA_N = 256;
 constexpr int UMMA_K = 16;
-constexpr int NUM_THREADS = 320;
-constexpr int EPI_WARPS = 8;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = UMMA_N * BK * 2;      // 32 KB
 constexpr int TMEM_COLS = 2 * UMMA_N;         // two accumulators
@@ -60,14 +59,38 @@ enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2, kBwdGelu = 3, kBwdSwiglu = 4 };
 // warp. Four 48 KB stages and two 2 KB buffers per warp fill the 227 KB
 // (measured on B300 against 3 stages + 4 buffers: 1.4 % faster on the
 // switch_top1 FFN, equal on the other workloads, and equal to 4 + 1).
-template <int STAGES_, int OUT_BUFS_>
+// EPIW is the number of epilogue warps (8 or 16; a multiple of four, since
+// warp w reads TMEM lanes 32 (w % 4) .. + 31): the CTA has 64 + 32 EPIW
+// threads.
+template <int STAGES_, int OUT_BUFS_, int EPIW_ = 8>
 struct Pipe {
   static constexpr int STAGES = STAGES_;
   static constexpr int OUT_BUFS = OUT_BUFS_;
+  static constexpr int EPIW = EPIW_;
+  static constexpr int THREADS = 64 + 32 * EPIW_;
 };
-using PipeShape = Pipe<4, 2>;
+#ifndef MOE_GEMM_EPIW
+#define MOE_GEMM_EPIW 8
+#endif
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES 4
+#endif
+#ifndef MOE_GEMM_OUTBUFS
+#define MOE_GEMM_OUTBUFS 2
+#endif
+#ifndef MOE_GEMM_PAIR_STAGES
+#define MOE_GEMM_PAIR_STAGES 6
+#endif
+#ifndef MOE_GEMM_PAIR_OUTBUFS
+#define MOE_GEMM_PAIR_OUTBUFS 2
+#endif
+// forward GEMMs
+using PipeShape = Pipe<MOE_GEMM_STAGES, MOE_GEMM_OUTBUFS, MOE_GEMM_EPIW>;
 // A CTA of a pair stages 32 KB per K step, so six stages fit.
-using PipePairShape = Pipe<6, 2>;
+using PipePairShape = Pipe<MOE_GEMM_PAIR_STAGES, MOE_GEMM_PAIR_OUTBUFS, MOE_GEMM_EPIW>;
+// the backward's GEMMs (their epilogue also reads the pre-activations)
+using PipeBwdShape = Pipe<4, 2, 8>;
+using PipeBwdPairShape = Pipe<6, 2, 8>;
 
 template <int STAGES>
 struct SmemTail {
@@ -95,10 +118,12 @@ __host__ __device__ constexpr int stage_b_bytes() {
 template <bool PAIR, class PIPE>
 constexpr size_t smem_bytes() {
   return 1024 /*align slack*/ + PIPE::STAGES * (A_BYTES + stage_b_bytes<PAIR>()) +
-         EPI_WARPS * PIPE::OUT_BUFS * STAGE_OUT_BYTES + sizeof(SmemTail<PIPE::STAGES>);
+         PIPE::EPIW * PIPE::OUT_BUFS * STAGE_OUT_BYTES + sizeof(SmemTail<PIPE::STAGES>);
 }
 static_assert(smem_bytes<false, PipeShape>() <= 227 * 1024, "shared memory");
 static_assert(smem_bytes<true, PipePairShape>() <= 227 * 1024, "shared memory");
+static_assert(smem_bytes<false, PipeBwdShape>() <= 227 * 1024, "shared memory");
+static_assert(smem_bytes<true, PipeBwdPairShape>() <= 227 * 1024, "shared memory");
 
 // GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
@@ -202,7 +227,7 @@ __device__ __forceinline__ TileInfo tile_info(const ST& st, const int32_t* __res
 // weights): per stage, boxes of [64 K rows x 64 N] side by side; with kb3 <
 // num_kb the K blocks from kb3 on come from tmB3 (W3 after W1).
 template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PIPE::THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB3,
@@ -217,6 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu;
   constexpr int STAGES = PIPE::STAGES;
   constexpr int OUT_BUFS = PIPE::OUT_BUFS;
+  constexpr int EPI_WARPS = PIPE::EPIW;
   constexpr int BM_T = PAIR ? 2 * BM : BM;              // rows of one tile
   constexpr int B_STAGE = stage_b_bytes<PAIR>();         // B bytes per CTA and stage
   constexpr uint32_t TX_BYTES = (PAIR ? 2u : 1u) * (uint32_t)(A_BYTES + B_STAGE);
@@ -365,8 +391,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) {
         aborted = true;
-        if (!PAIR) {
-          // let the copies already issued land before the CTA exits
+        // let the copies already issued land before the CTA exits (each wait
+        // time-limited). A pair's fills, both CTAs', complete on the even
+        // CTA's `full` barriers, so only rank 0 can watch them land; the odd
+        // CTA relies on the closing delay below.
+        if (!PAIR || rank == 0) {
           int s = stage;
           uint32_t ph = phase;
           for (int i = 0; i < STAGES && i < issued; ++i) {
@@ -452,10 +481,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ================= epilogue (warps 2..9)
+    // ================= epilogue (warps 2 .. 1 + EPI_WARPS)
     const int ew = warp - 2;
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-    const int half = ew >> 2;              // which half of the tile's columns
+    const int part = ew >> 2;              // which part (of EPI_WARPS / 4) of the tile's columns
     const uint32_t empty_cl0 = PAIR ? cluster_addr(&st.tmem_empty[0], 0) : 0u;
     const uint32_t empty_cl1 = PAIR ? cluster_addr(&st.tmem_empty[1], 0) : 0u;
     int acc = 0;
@@ -483,21 +512,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // row scatter) direct stores of the valid rows
       const bool warp_full = !SCATTER && (wrow0 + 32 <= ti.mend);
       uint8_t* my_out0 = sOut + ew * OUT_BUFS * STAGE_OUT_BYTES;
-      // The warp's whole slice of the accumulator (128 fp32 columns, or 64
-      // gate + 64 up columns for SwiGLU) goes to registers with one wait, and
-      // the TMEM buffer is handed back to the MMA before the activation and
-      // the stores.
-      constexpr int OUTC = MODE == kSwiglu ? 64 : 128;  // output columns per warp
-      const int cbase = OUTC * half;                     // tile-local first column
-      uint32_t r[128];
+      // The warp's whole slice of the accumulator (UMMA_N / parts fp32
+      // columns, or as many gate and as many up columns for SwiGLU) goes to
+      // registers with one wait, and the TMEM buffer is handed back to the
+      // MMA before the activation and the stores.
+      constexpr int PARTS = EPI_WARPS / 4;
+      constexpr int OUTC = (MODE == kSwiglu ? 128 : 256) / PARTS;  // output columns per warp
+      constexpr int NREG = MODE == kSwiglu ? 2 * OUTC : OUTC;     // accumulator columns per warp
+      const int cbase = OUTC * part;                               // tile-local first column
+      uint32_t r[NREG];
       if (MODE == kSwiglu) {
-        tmem_ld32(t_row + (uint32_t)cbase, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(t_row + (uint32_t)(cbase + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_ld32(t_row + (uint32_t)(128 + cbase), *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-        tmem_ld32(t_row + (uint32_t)(128 + cbase + 32), *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+#pragma unroll
+        for (int ch = 0; ch < OUTC / 32; ++ch) {
+          tmem_ld32(t_row + (uint32_t)(cbase + 32 * ch),
+                    *reinterpret_cast<uint32_t(*)[32]>(&r[32 * ch]));
+          tmem_ld32(t_row + (uint32_t)(128 + cbase + 32 * ch),
+                    *reinterpret_cast<uint32_t(*)[32]>(&r[OUTC + 32 * ch]));
+        }
       } else {
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
+        for (int ch = 0; ch < OUTC / 32; ++ch)
           tmem_ld32(t_row + (uint32_t)(cbase + 32 * ch), *reinterpret_cast<uint32_t(*)[32]>(&r[32 * ch]));
       }
       tmem_ld_wait();
@@ -520,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (MODE == kSwiglu) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            v[j] = silu_f(__uint_as_float(r[32 * ch + j])) * __uint_as_float(r[64 + 32 * ch + j]);
+            v[j] = silu_f(__uint_as_float(r[32 * ch + j])) * __uint_as_float(r[OUTC + 32 * ch + j]);
         } else if (BWD) {
           // dh for 32 columns of this row; the saved pre-activations of the
           // same row and columns (gate a and up v for SwiGLU: v at column N + n)
@@ -625,7 +659,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   if (PAIR) {
     // A CTA that gave up may still have copies in flight that signal or fill
-    // the pair's shared memory; give them time to land before either exits.
+    // the pair's shared memory. Rank 0 has waited for the fills it armed; the
+    // odd CTA cannot observe its own, so both give them a further 200 us to
+    // land before either exits.
     if (__syncthreads_or(aborted ? 1 : 0)) {
       const uint64_t t0 = globaltimer();
       while (globaltimer() - t0 < 200000ull) {
@@ -725,7 +761,7 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
     if (PAIR) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * units);
-      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.blockDim = dim3(PIPE::THREADS);
       cfg.dynamicSmemBytes = SMEM_BYTES;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -746,7 +782,7 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   int64_t units = tiles_bound < max_units[dev] ? tiles_bound : max_units[dev];
   if (units < 1) units = 1;
   const unsigned grid = (unsigned)(PAIR ? 2 * units : units);
-  return launch_pdl_cluster(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
+  return launch_pdl_cluster(kernel, dim3(grid), dim3(PIPE::THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
                             b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
                             static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale,
                             static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N, kb3);
@@ -760,20 +796,23 @@ cudaError_t launch_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                         int32_t* hdr, const int32_t* o_rows, const float* o_scale,
                         cudaStream_t s, const void* pre = nullptr, int ldo = 0, int kb3 = -1) {
   if (!BMN || kb3 < 0) kb3 = (K + BK - 1) / BK;
+  constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu || BMN;
+  using PP = typename std::conditional<BWD, PipeBwdPairShape, PipePairShape>::type;
+  using PS = typename std::conditional<BWD, PipeBwdShape, PipeShape>::type;
   if (pair)
-    return launch_gemm_p<MODE, SCATTER, true, PipePairShape, BMN>(
-        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, kb3,
-        s);
-  return launch_gemm_p<MODE, SCATTER, false, PipeShape, BMN>(a, b, b3, o, offset, E, N, K, bias,
-                                                             out, rows_bound, hdr, o_rows,
-                                                             o_scale, pre, ldo, kb3, s);
+    return launch_gemm_p<MODE, SCATTER, true, PP, BMN>(a, b, b3, o, offset, E, N, K, bias, out,
+                                                       rows_bound, hdr, o_rows, o_scale, pre, ldo,
+                                                       kb3, s);
+  return launch_gemm_p<MODE, SCATTER, false, PS, BMN>(a, b, b3, o, offset, E, N, K, bias, out,
+                                                      rows_bound, hdr, o_rows, o_scale, pre, ldo,
+                                                      kb3, s);
 }
 
 }  // namespace
 
 // Whether clusters of two CTAs of the pair kernel can be resident on the
-// current device (every pair instantiation has the same shared memory and
-// block size). Queried once per device.
+// current device (every pair instantiation takes one CTA per SM: nearly all
+// of the shared memory). Queried once per device.
 static bool pairs_fit() {
   static int fit[64] = {};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
@@ -786,7 +825,7 @@ static bool pairs_fit() {
                              (int)SMEM_BYTES) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2);
-      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.blockDim = dim3(PipePairShape::THREADS);
       cfg.dynamicSmemBytes = SMEM_BYTES;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -842,7 +881,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
     e = launch_gemm<kGelu, false>(pair, mx, mw1, mw3, moh, offset, c.E, c.H, c.d, b1, h,
                                   rows_bound, hdr, nullptr, nullptr, s);
   if (e != cudaSuccess) return e;
-  if (fz && fz->between && (e = cudaEventRecord(fz->between, s)) != cudaSuccess) return e;
+  if (fz && fz->between && (e = record_stage_event(fz->between, s)) != cudaSuccess) return e;
   const void* b2e = swiglu ? nullptr : b2;
   if (scatter)
     return launch_gemm<kPlain, true>(pair, mh, mw2, mw2, moy, offset, c.E, c.d, c.H, b2e, fz->y,

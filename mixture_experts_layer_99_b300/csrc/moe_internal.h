@@ -59,6 +59,18 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Records a stage-boundary event on s. Inside a stream capture the record
+// becomes an event node of the graph (cudaEventRecordExternal), so the event
+// is recorded, and can be timed, each time the graph is replayed.
+inline cudaError_t record_stage_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  return cudaEventRecord(ev, s);
+}
+
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 8;
 
@@ -94,13 +106,18 @@ inline int router_grid(const moe_config_t& c, int /*unused*/) {
   return tiles < kRouterMaxBlocks ? tiles : kRouterMaxBlocks;
 }
 
-// Tensor-core router: 128-token tiles, at most one CTA per SM of a 148-SM
-// B300 (a fixed bound, so the per-CTA partial sums do not depend on the
-// device).
+// Tensor-core router: tiles of 128 tokens (the MMA's M), at most one CTA per
+// SM of a 148-SM B300 (a fixed bound, so the per-CTA partial sums do not
+// depend on the device). Cutting the batch into as many smaller tiles as keep
+// all 148 SMs busy (147 tiles of 112 tokens at T = 16384 instead of 128 of
+// 128) measured no faster on B300: the tile loads are bound by DRAM, not by
+// the number of SMs pulling.
 constexpr int kRouterTcTile = 128;
 constexpr int kRouterTcMaxBlocks = 148;
+inline int router_tc_rows(const moe_config_t&) { return kRouterTcTile; }
 inline int router_tc_tiles(const moe_config_t& c) {
-  return (c.T + kRouterTcTile - 1) / kRouterTcTile;
+  const int rows = router_tc_rows(c);
+  return (c.T + rows - 1) / rows;
 }
 inline int router_tc_grid(const moe_config_t& c) {
   const int t = router_tc_tiles(c);
@@ -223,7 +240,7 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
                               float* dz, void* dz_bf16, int Kp, cudaStream_t s);
 int bwd_wg_group_tokens(const moe_config_t& c);
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const void* dxr, void* dx, cudaStream_t s);
+                          const void* dxr, void* dx, cudaStream_t s, const void* dxs = nullptr);
 cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzb, int Kp,
                           const void* x, int32_t* goff, float* part, float* dWg, float* dbias,
                           int32_t* hdr, cudaStream_t s);

@@ -27,7 +27,7 @@ constexpr int NT = 256;          // threads per block
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(NT) router_simt_kernel(
     const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias,
-    const float* __restrict__ noise, float tau, int T, int d, int E, int k,
+    const float* __restrict__ noise, float noise_scale, float tau, int T, int d, int E, int k,
     float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
     float* __restrict__ partial) {
   constexpr int EPAD = 16 * EP;
@@ -79,17 +79,42 @@ __global__ void __launch_bounds__(NT) router_simt_kernel(
       }
     }
     __syncthreads();
-    // selection keys l = (z + b + g) / tau
+    // selection keys l = (z + b + s g) / tau, s = 1 or noise_scale times the
+    // population standard deviation of the token's E logits z + b (the 16
+    // threads of a token's row, lanes of one half-warp, sum in a fixed order)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int r = 2 * ty + i, t = t0 + r;
+      float sn = 1.f;
+      if (bias) {
+#pragma unroll
+        for (int c = 0; c < EP; ++c)
+          if (tx + 16 * c < E) acc[i][c] += bias[tx + 16 * c];
+      }
+      if (noise && noise_scale > 0.f) {
+        float s1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < EP; ++c)
+          if (tx + 16 * c < E) s1 += acc[i][c];
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        const float mean = s1 / (float)E;
+        float s2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < EP; ++c) {
+          const float dv = acc[i][c] - mean;
+          if (tx + 16 * c < E) s2 = fmaf(dv, dv, s2);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        sn = noise_scale * sqrtf(s2 / (float)E);
+      }
 #pragma unroll
       for (int c = 0; c < EP; ++c) {
         const int e = tx + 16 * c;
         float v = acc[i][c];
         if (e < E && t < T) {
-          if (bias) v += bias[e];
-          if (noise) v += noise[(size_t)t * E + e];
+          if (noise) v = fmaf(sn, noise[(size_t)t * E + e], v);
           v = v / tau;
         }
         ls[r * LDL + e] = v;
@@ -206,9 +231,10 @@ cudaError_t launch_router_t(const moe_config_t& c, const void* x, const void* Wg
   const Tin* xp = static_cast<const Tin*>(x);
   const Tin* wp = static_cast<const Tin*>(Wg);
   const int epad = (c.E + 15) / 16;
-#define MOE_ROUTER_CASE(EPV)                                                             \
-  router_simt_kernel<Tin, EPV><<<grid, NT, 0, s>>>(xp, wp, bias, noise, c.tau, c.T, c.d, \
-                                                   c.E, c.k, logits, idx, gate, partial)
+#define MOE_ROUTER_CASE(EPV)                                                              \
+  router_simt_kernel<Tin, EPV><<<grid, NT, 0, s>>>(xp, wp, bias, noise, c.noise_scale, c.tau, \
+                                                   c.T, c.d, c.E, c.k, logits, idx, gate,     \
+                                                   partial)
   if (epad <= 1) MOE_ROUTER_CASE(1);
   else if (epad <= 2) MOE_ROUTER_CASE(2);
   else if (epad <= 4) MOE_ROUTER_CASE(4);

@@ -1,6 +1,8 @@
 // Fused router on the tcgen05 tensor cores for bf16 tokens and E <= 64.
 //
-// logits l = (x Wg^T + b + g) / tau, softmax p = softmax(l), the k largest
+// logits l = (x Wg^T + b + s g) / tau (s = 1, or a scale times the token's
+// logit standard deviation: std-scaled noise, section 3.3 of the article
+// below), softmax p = softmax(l), the k largest
 // logits (descending, ties to the lower expert index), renormalised gates
 // g_j = p_{K_j} / sum_m p_{K_m}, per-CTA sums of p for P_i and per-tile
 // selection counts for the dispatch. This is the gate of the kwkr.cn MoE
@@ -147,22 +149,45 @@ __device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi)
 // p (fixed order). v holds the thread's Q raw logits on entry.
 template <int EP, int KM>
 __device__ __forceinline__ void router_tile_epilogue(
-    float (&v)[EP / TPT], int tile, int r, int p, int etid, const float* __restrict__ bias,
-    const float* __restrict__ noise, float tau, int T, int E, int k, float* __restrict__ logits,
-    int32_t* __restrict__ idx, float* __restrict__ gate, int32_t* __restrict__ tile_hist,
-    EpiSmem<EP>& es) {
+    float (&v)[EP / TPT], int tile, int tile_rows, int r, int p, int etid,
+    const float* __restrict__ bias,
+    const float* __restrict__ noise, float noise_scale, float tau, int T, int E, int k,
+    float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
+    int32_t* __restrict__ tile_hist, EpiSmem<EP>& es) {
   constexpr int Q = EP / TPT;
-  const int t = tile * BM + r;
-  const bool valid = t < T;
+  const int t = tile * tile_rows + r;
+  const bool valid = r < tile_rows && t < T;
   const int e0 = p * Q;
   const bool vec4 = (E & 3) == 0;  // rows of [T, E] fp32 arrays are 16-byte aligned
-  // selection keys l = (z + b + g) / tau (one reciprocal; tau = 1 leaves them as they are)
-  if (valid) {
-    if (bias) {
+  // selection keys l = (z + b + s g) / tau (one reciprocal; tau = 1 leaves them as they are)
+  if (valid && bias) {
 #pragma unroll
-      for (int q = 0; q < Q; ++q)
-        if (e0 + q < E) v[q] += __ldg(bias + e0 + q);
+    for (int q = 0; q < Q; ++q)
+      if (e0 + q < E) v[q] += __ldg(bias + e0 + q);
+  }
+  // noise strength: 1, or noise_scale times the population standard deviation
+  // of the token's E logits (z + b), summed by the token's four threads in a
+  // fixed order (every lane runs the shuffles)
+  float sn = 1.f;
+  if (noise && noise_scale > 0.f) {
+    float s1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+      if (e0 + q < E) s1 += v[q];
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    const float mean = s1 / (float)E;
+    float s2 = 0.f;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const float dv = v[q] - mean;
+      if (e0 + q < E) s2 = fmaf(dv, dv, s2);
     }
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    sn = noise_scale * sqrtf(s2 / (float)E);
+  }
+  if (valid) {
     if (noise) {
       const float* nr = noise + (size_t)t * E + e0;
       if (vec4) {
@@ -170,16 +195,16 @@ __device__ __forceinline__ void router_tile_epilogue(
         for (int q = 0; q < Q; q += 4) {
           if (e0 + q < E) {
             const float4 w = __ldg(reinterpret_cast<const float4*>(nr + q));
-            v[q] += w.x;
-            v[q + 1] += w.y;
-            v[q + 2] += w.z;
-            v[q + 3] += w.w;
+            v[q] = fmaf(sn, w.x, v[q]);
+            v[q + 1] = fmaf(sn, w.y, v[q + 1]);
+            v[q + 2] = fmaf(sn, w.z, v[q + 2]);
+            v[q + 3] = fmaf(sn, w.w, v[q + 3]);
           }
         }
       } else {
 #pragma unroll
         for (int q = 0; q < Q; ++q)
-          if (e0 + q < E) v[q] += __ldg(nr + q);
+          if (e0 + q < E) v[q] = fmaf(sn, __ldg(nr + q), v[q]);
       }
     }
     if (tau != 1.f) {
@@ -328,11 +353,12 @@ template <int EP, int KM, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const float* __restrict__ bias,
-                     const float* __restrict__ noise, float tau, int T, int d, int E, int k,
+                     const float* __restrict__ noise, float noise_scale, float tau, int T,
+                     int d, int E, int k,
                      float* __restrict__ logits, int32_t* __restrict__ idx,
                      float* __restrict__ gate, float* __restrict__ partial,
                      int32_t* __restrict__ tile_hist, int32_t* __restrict__ hdr, int ksplit,
-                     int kb_per_split, float* __restrict__ split_part) {
+                     int kb_per_split, int tile_rows) {
   using Cfg = RouterCfg<EP>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -371,7 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_wait();
   const uint32_t tmem_base = st.tmem_base;
   // work unit u = (tile, split): K blocks [split * kb_per_split, ...) of the tile
-  const int ntiles = (T + BM - 1) / BM;
+  const int ntiles = (T + tile_rows - 1) / tile_rows;
   const int nunits = ntiles * ksplit;
   const int num_kb = (d + BK - 1) / BK;
   volatile int* abort_flag = &st.abort_flag;
@@ -381,6 +407,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const uint32_t stage_tx = (uint32_t)(tile_rows * BK * 2 + Cfg::B_BYTES);
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const int tile = u / ksplit, split = u % ksplit;
         const int kb0 = split * kb_per_split;
@@ -390,8 +417,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(&st.full[stage], Cfg::STAGE);
-          tma_load_2d(sA + stage * A_BYTES, &tmX, &st.full[stage], kb * BK, tile * BM);
+          mbar_expect_tx(&st.full[stage], stage_tx);
+          tma_load_2d(sA + stage * A_BYTES, &tmX, &st.full[stage], kb * BK, tile * tile_rows);
           tma_load_2d(sB + stage * Cfg::B_BYTES, &tmW, &st.full[stage], kb * BK, 0);
           ++issued;
           if (++stage == STAGES) {
@@ -499,8 +526,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!SPLIT) {
         float v[Q];
         load_quarter<EP>(st.epi, r, p, v);
-        router_tile_epilogue<EP, KM>(v, tile, r, p, etid, bias, noise, tau, T, E, k, logits, idx,
-                                     gate, tile_hist, st.epi);
+        router_tile_epilogue<EP, KM>(v, tile, tile_rows, r, p, etid, bias, noise, noise_scale,
+                                     tau, T, E, k, logits, idx, gate, tile_hist, st.epi);
       }
     }
     if (!SPLIT)
@@ -556,8 +583,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       load_quarter<EP>(st.epi, r, p, v);
       if (etid < EP) st.epi.hist[etid] = 0;
       epi_bar();  // counts zeroed before the epilogue's atomics
-      router_tile_epilogue<EP, KM>(v, tile, r, p, etid, bias, noise, tau, T, E, k, logits, idx,
-                                   gate, tile_hist, st.epi);
+      router_tile_epilogue<EP, KM>(v, tile, BM, r, p, etid, bias, noise, noise_scale, tau, T, E,
+                                   k, logits, idx, gate, tile_hist, st.epi);
       for (int e = etid; e < E; e += EPI_THREADS) partial[(size_t)tile * E + e] = st.epi.part[e];
     }
   }
@@ -626,16 +653,18 @@ cudaError_t launch_ep_km(const moe_config_t& c, const CUtensorMap& mx, const CUt
   if (sp.ksplit == 1) {
     if ((e = set_smem_attr<EP, KM, false>()) != cudaSuccess) return e;
     return launch_pdl(router_tc_kernel<EP, KM, false>, dim3(router_tc_grid(c)),
-                      dim3(NUM_THREADS), router_smem_bytes<EP>(), s, mx, mw, bias, noise, c.tau,
-                      c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr, 1,
-                      sp.kb_per_split, (float*)nullptr);
+                      dim3(NUM_THREADS), router_smem_bytes<EP>(), s, mx, mw, bias, noise,
+                      c.noise_scale, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial,
+                      tile_hist, hdr, 1,
+                      sp.kb_per_split, router_tc_rows(c));
   }
   if ((e = set_smem_attr<EP, KM, true>()) != cudaSuccess) return e;
   const int units = router_tc_tiles(c) * sp.ksplit;  // one cluster of ksplit CTAs per tile
   return launch_pdl_cluster(router_tc_kernel<EP, KM, true>, dim3(units), dim3(NUM_THREADS),
-                            router_smem_bytes<EP>(), sp.ksplit, s, mx, mw, bias, noise, c.tau,
-                            c.T, c.d, c.E, c.k, logits, idx, gate, partial, tile_hist, hdr,
-                            sp.ksplit, sp.kb_per_split, (float*)nullptr);
+                            router_smem_bytes<EP>(), sp.ksplit, s, mx, mw, bias, noise,
+                            c.noise_scale, c.tau, c.T, c.d, c.E, c.k, logits, idx, gate, partial,
+                            tile_hist, hdr,
+                            sp.ksplit, sp.kb_per_split, (int)kRouterTcTile);
 }
 
 // k <= 2 sorts candidate lists of two entries, larger k lists of eight.
@@ -645,7 +674,8 @@ cudaError_t launch_ep(const moe_config_t& c, const void* x, const void* Wg, cons
                       float* partial, int32_t* tile_hist, float* split_part, int32_t* hdr,
                       cudaStream_t s) {
   CUtensorMap mx, mw;
-  if (!map_rows(&mx, x, c.d, c.T, BM) || !map_rows(&mw, Wg, c.d, c.E, EP))
+  if (!map_rows(&mx, x, c.d, c.T, (uint32_t)router_tc_rows(c)) ||
+      !map_rows(&mw, Wg, c.d, c.E, EP))
     return cudaErrorInvalidValue;
   (void)split_part;
   if (c.k <= 2)

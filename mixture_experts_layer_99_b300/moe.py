@@ -31,7 +31,8 @@ EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspa
             "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
             "moe_layer_forward_launch_count", "moe_layer_forward_profiled",
             "moe_workspace_size_shared", "moe_layer_forward_shared", "moe_dispatch_static_scratch",
-            "moe_workspace_size_backward", "moe_layer_backward"]
+            "moe_workspace_size_backward", "moe_layer_backward",
+            "moe_workspace_size_backward_shared", "moe_layer_backward_shared"]
 
 
 class MoEError(RuntimeError):
@@ -44,11 +45,12 @@ class MoEError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("T", c_int32), ("d", c_int32), ("E", c_int32), ("k", c_int32),
                 ("H", c_int32), ("capacity", c_int32), ("dtype", c_int32),
-                ("act", c_int32), ("tau", c_float)]
+                ("act", c_int32), ("tau", c_float), ("noise_scale", c_float)]
 
     def __repr__(self):
         return (f"Config(T={self.T}, d={self.d}, E={self.E}, k={self.k}, H={self.H}, "
-                f"C={self.capacity}, dtype={self.dtype}, act={self.act}, tau={self.tau})")
+                f"C={self.capacity}, dtype={self.dtype}, act={self.act}, tau={self.tau}, "
+                f"noise_scale={self.noise_scale})")
 
 
 class LayerInputs(ctypes.Structure):
@@ -72,6 +74,11 @@ class LayerOutputs(ctypes.Structure):
 class LayerGrads(ctypes.Structure):
     _fields_ = [("dx", c_void_p), ("dWg", c_void_p), ("dbias", c_void_p), ("dW1", c_void_p),
                 ("dW3", c_void_p), ("dW2", c_void_p), ("db1", c_void_p), ("db2", c_void_p)]
+
+
+class SharedGrads(ctypes.Structure):
+    _fields_ = [("dW1", c_void_p), ("dW3", c_void_p), ("dW2", c_void_p), ("db1", c_void_p),
+                ("db2", c_void_p)]
 
 
 _LIB = None
@@ -117,6 +124,11 @@ def lib():
         "moe_layer_backward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs), vp,
                                          ctypes.c_float, POINTER(LayerGrads), vp, c_size_t, vp,
                                          c_size_t, vp]),
+        "moe_workspace_size_backward_shared": (c_int32, [cfgp, c_int32, POINTER(c_size_t)]),
+        "moe_layer_backward_shared": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(SharedExpert),
+                                                POINTER(LayerOutputs), vp, ctypes.c_float,
+                                                POINTER(LayerGrads), POINTER(SharedGrads), vp,
+                                                c_size_t, vp, c_size_t, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -136,15 +148,17 @@ def capacity(c, k: int, T: int, E: int) -> int:
     return v
 
 
-def make_config(T, d, E, k, H, capacity_, dtype="bf16", act="gelu", tau=1.0) -> Config:
+def make_config(T, d, E, k, H, capacity_, dtype="bf16", act="gelu", tau=1.0,
+                noise_scale=0.0) -> Config:
     return Config(T, d, E, k, H, capacity_, MOE_F32 if dtype == "f32" else MOE_BF16,
-                  MOE_ACT_GELU if act == "gelu" else MOE_ACT_SWIGLU, float(tau))
+                  MOE_ACT_GELU if act == "gelu" else MOE_ACT_SWIGLU, float(tau),
+                  float(noise_scale))
 
 
 def config_from_workload(w, T: Optional[int] = None) -> Config:
     T = w.T if T is None else T
     return make_config(T, w.d, w.E, w.k, w.H, capacity(w.c, w.k, T, w.E), w.dtype, w.act,
-                       w.tau)
+                       w.tau, w.noise_scale)
 
 
 def _dt(cfg):
@@ -450,3 +464,63 @@ def layer_backward(cfg, inp: dict, fwd: dict, dy, alpha: float = 0.0, *, ws, bws
           _ptr(dy), ctypes.c_float(alpha), ctypes.byref(lg), _ptr(ws), ws.numel(), _ptr(bws),
           bws.numel(), _stream(dev))
     return g
+
+
+def _shared_expert(cfg, shared: dict, dev) -> SharedExpert:
+    dt = _dt(cfg)
+    Hs = shared["W1"].shape[0]
+    _need(shared["W1"], "shared W1", dt, (Hs, cfg.d), dev)
+    _need(shared["W2"], "shared W2", dt, (cfg.d, Hs), dev)
+    _opt(shared.get("W3"), "shared W3", dt, (Hs, cfg.d), dev)
+    _opt(shared.get("b1"), "shared b1", dt, (Hs,), dev)
+    _opt(shared.get("b2"), "shared b2", dt, (cfg.d,), dev)
+    return SharedExpert(Hs, _ptr(shared["W1"]), _ptr(shared.get("W3")), _ptr(shared["W2"]),
+                        _ptr(shared.get("b1")), _ptr(shared.get("b2")))
+
+
+def workspace_backward_shared(cfg: Config, H_shared: int, device="cuda") -> torch.Tensor:
+    """The backward workspace of a layer with a shared expert (256-byte
+    aligned, header zeroed)."""
+    n = c_size_t(0)
+    _call("moe_workspace_size_backward_shared", ctypes.byref(cfg), H_shared, ctypes.byref(n))
+    ws = torch.empty(n.value + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n.value]
+    _call("moe_workspace_init", c_void_p(ws.data_ptr()), n.value, c_void_p(_stream(ws.device)))
+    return ws
+
+
+def alloc_shared_grads(cfg, shared: dict, device):
+    """fp32 gradient buffers for the shared expert's weights (dW3, db1, db2
+    only where the shared expert has them)."""
+    Hs, d = shared["W1"].shape[0], cfg.d
+    f32 = dict(dtype=torch.float32, device=device)
+    g = dict(dW1=torch.empty(Hs, d, **f32), dW2=torch.empty(d, Hs, **f32))
+    if shared.get("W3") is not None:
+        g["dW3"] = torch.empty(Hs, d, **f32)
+    if shared.get("b1") is not None:
+        g["db1"] = torch.empty(Hs, **f32)
+    if shared.get("b2") is not None:
+        g["db2"] = torch.empty(d, **f32)
+    return g
+
+
+def layer_backward_shared(cfg, inp: dict, shared: dict, fwd: dict, dy, alpha: float = 0.0, *,
+                          ws, bws=None, grads: Optional[dict] = None,
+                          shared_grads: Optional[dict] = None):
+    """Backward of a layer_forward_shared call (workspace ``ws``, outputs
+    ``fwd``). Returns (gradient dict, shared-expert gradient dict)."""
+    dev = inp["x"].device
+    li = _layer_inputs(cfg, inp, dev)
+    se = _shared_expert(cfg, shared, dev)
+    _need(dy, "dy", _dt(cfg), (cfg.T, cfg.d), dev)
+    lo = LayerOutputs(*[_ptr(fwd.get(n)) for n, _ in LayerOutputs._fields_])
+    g = alloc_grads(cfg, inp, dev) if grads is None else grads
+    sg = alloc_shared_grads(cfg, shared, dev) if shared_grads is None else shared_grads
+    lg = LayerGrads(*[_ptr(g.get(n)) for n, _ in LayerGrads._fields_])
+    lsg = SharedGrads(*[_ptr(sg.get(n)) for n, _ in SharedGrads._fields_])
+    bws = workspace_backward_shared(cfg, se.H, dev) if bws is None else bws
+    _call("moe_layer_backward_shared", ctypes.byref(cfg), ctypes.byref(li), ctypes.byref(se),
+          ctypes.byref(lo), _ptr(dy), ctypes.c_float(alpha), ctypes.byref(lg), ctypes.byref(lsg),
+          _ptr(ws), ws.numel(), _ptr(bws), bws.numel(), _stream(dev))
+    return g, sg

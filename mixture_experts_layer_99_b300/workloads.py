@@ -25,10 +25,15 @@ The five workloads follow the shapes the MoE pages use:
   1024->2048->1024), c=1.25, and Gaussian router noise of standard deviation
   0.05 added to the logits (the ``noise_std`` of the kwkr.cn MoE article,
   section 3.3, whose typical range is 0.01 to 0.1).
+* ``sweep_std_noise`` - the same layer with the refined noise of that
+  section: standard normal noise whose strength is 0.1 times each token's
+  standard deviation of its logits (the router applies the scaling; the
+  drawn tensor is N(0, 1)).
 
 Draw order (one ``torch.Generator('cpu')`` per workload, seeded): x, W_g, W1,
-W3 (SwiGLU only), W2, then the router noise (u for Gumbel noise, or a
-standard normal draw scaled by ``noise_std``). All normal draws are fp32
+W3 (SwiGLU only), W2, then the router noise (u for Gumbel noise, a
+standard normal draw scaled by ``noise_std``, or an unscaled standard normal
+draw for std-scaled noise). All normal draws are fp32
 ``randn``; weights are scaled by 1/sqrt(fan_in) and then cast to the workload
 dtype. Weights use the ``nn.Linear`` storage convention [out, in]:
 W_g [E, d], W1 and W3 [E, H, d], W2 [E, d, H].
@@ -56,8 +61,8 @@ class Workload:
     c: Fraction              # capacity factor, exact
     expert_bias: bool = False    # b1 [E,H], b2 [E,d] present (zeros)
     router_bias: Optional[str] = None   # None or "zipf"
-    noise: Optional[str] = None         # None, "gumbel" or "gaussian"
-    noise_std: float = 0.0              # standard deviation of "gaussian" noise
+    noise: Optional[str] = None         # None, "gumbel", "gaussian" or "gaussian_std"
+    noise_std: float = 0.0              # std of "gaussian" noise; the scale of "gaussian_std"
     tau: float = 1.0
     seed: int = 0
     shared_H: int = 0                   # > 0: a shared expert of this hidden size
@@ -73,6 +78,13 @@ class Workload:
     @property
     def nmat(self):
         return 3 if self.act == "swiglu" else 2
+
+    @property
+    def noise_scale(self) -> float:
+        """The router's noise_scale: > 0 for noise whose strength follows each
+        token's logit standard deviation ("gaussian_std"), else 0 (the noise
+        tensor is added as drawn)."""
+        return self.noise_std if self.noise == "gaussian_std" else 0.0
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -93,6 +105,11 @@ WORKLOADS = {
     "sweep_e16_k4": Workload("sweep_e16_k4", T=8192, d=1024, E=16, k=4, H=2048,
                              act="gelu", dtype="bf16", c=Fraction(5, 4),
                              noise="gaussian", noise_std=0.05),
+    # the same sweep point with std-scaled router noise (strength 0.1 times
+    # each token's logit standard deviation)
+    "sweep_std_noise": Workload("sweep_std_noise", T=8192, d=1024, E=16, k=4, H=2048,
+                                act="gelu", dtype="bf16", c=Fraction(5, 4),
+                                noise="gaussian_std", noise_std=0.1),
     # the long-tail layer plus one always-on shared expert of the same width
     "longtail_shared": Workload("longtail_shared", T=32768, d=2048, E=64, k=2, H=1408,
                                 act="swiglu", dtype="bf16", c=Fraction(2),
@@ -145,6 +162,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
         noise = (-torch.log(-torch.log(u))).to(torch.float32)
     elif w.noise == "gaussian":
         noise = _randn(gen, (w.T, w.E), w.noise_std, torch.float32)
+    elif w.noise == "gaussian_std":   # N(0, 1); the router scales it per token
+        noise = _randn(gen, (w.T, w.E), 1.0, torch.float32)
     out = dict(x=x, Wg=Wg, W1=W1, W3=W3, W2=W2, b1=b1, b2=b2, bias=bias, noise=noise)
     if w.shared_H > 0:   # drawn last, so the routed inputs do not change
         Hs = w.shared_H

@@ -61,7 +61,8 @@ def check_layer(w: W.Workload, device, n_sample=None, seed=None, inp=None):
     C = ORC.capacity(w.c, w.k, w.T, w.E)
     assert cfg.capacity == C
     lg = out["logits"].cpu().numpy()                     # fp32 keys
-    ref_l = ORC.router_logits(inp["x"], inp["Wg"], inp["bias"], inp["noise"], w.tau)
+    ref_l = ORC.router_logits(inp["x"], inp["Wg"], inp["bias"], inp["noise"], w.tau,
+                              w.noise_scale)
     e_l = rel_err(lg, ref_l)
     assert e_l <= TOL_LOGITS[w.dtype], f"logits rel err {e_l}"
     r = ORC.route_from_logits(lg, w.k, C)

@@ -34,7 +34,9 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     L = moe.lib()
-    assert L.moe_abi_version() >= 100
+    # 1.01: moe_config_t carries noise_scale (std-scaled router noise)
+    assert L.moe_abi_version() == 101
+    assert ctypes.sizeof(moe.Config) == 10 * 4
     for code in range(6):
         assert L.moe_status_string(code)
     assert L.moe_status_string(99) == b"unknown status"
@@ -62,7 +64,8 @@ def _cfg(**kw):
 
 @pytest.mark.parametrize("bad", [dict(T=0), dict(E=0), dict(k=0), dict(k=5), dict(d=60),
                                  dict(H=100), dict(capacity_=0), dict(tau=0.0),
-                                 dict(tau=float("nan")), dict(d=63, dtype="f32")])
+                                 dict(tau=float("nan")), dict(d=63, dtype="f32"),
+                                 dict(noise_scale=-0.1), dict(noise_scale=float("inf"))])
 def test_invalid_config_rejected(bad):
     with pytest.raises(moe.MoEError) as ei:
         moe.workspace_size(_cfg(**bad))

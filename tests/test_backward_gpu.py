@@ -32,6 +32,8 @@ CASES = {
     "ragged_dims": (W.small(WL["switch_top1"], T=600, d=136, H=200, E=5, k=2), 0.3, True),
     # SwiGLU with H not a multiple of 64: dxd reads the transposed [W1^T | W3^T]
     "swiglu_ragged_h": (W.small(WL["mixtral"], T=640, d=136, H=200, E=5), 0.1, False),
+    # std-scaled router noise: its strength carries no gradient
+    "std_noise": (W.small(WL["sweep_std_noise"], T=1500, d=256, H=256), 0.1, False),
 }
 
 
@@ -57,7 +59,7 @@ def test_backward_matches_oracle(name):
     w, alpha, with_bias = CASES[name]
     inp, dy, cfg, out, grads = _run(w, alpha, with_bias)
     ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, alpha, w.tau,
-                          logits=out["logits"].cpu().numpy())
+                          logits=out["logits"].cpu().numpy(), noise_scale=w.noise_scale)
     # the oracle followed the GPU's routing
     np.testing.assert_array_equal(ref["route"]["slot_of"], out["slot_of"].cpu().numpy())
     pairs = dict(dx=ref["dx"], dWg=ref["dWg"], dbias=ref["dbias"], dW1=ref["dW1"],
@@ -71,6 +73,60 @@ def test_backward_matches_oracle(name):
     print(name, {k: f"{v:.2e}" for k, v in errs.items()})
     for key, e in errs.items():
         assert e <= TOL[key], (key, e)
+
+
+SHARED_CASES = {
+    # SwiGLU long tail plus a shared expert (drops, bias, Gumbel noise)
+    "longtail_shared_small": W.small(WL["longtail_shared"], T=2000, d=128, H=192).with_(
+        shared_H=256),
+    # GELU, k = 2, with nonzero biases on the routed and the shared experts
+    "gelu_shared_bias": W.small(WL["sweep_e16_k4"], T=1500, d=256, H=256, k=2).with_(
+        shared_H=320, expert_bias=True),
+    # SwiGLU shared expert whose H is not a multiple of 64 (transposed [W1; W3])
+    "swiglu_shared_ragged_h": W.small(WL["mixtral"], T=700, d=136, H=128, E=4).with_(
+        shared_H=200),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHARED_CASES))
+def test_backward_shared_expert_matches_oracle(name):
+    """moe_layer_backward_shared: the routed gradients as without the shared
+    expert, plus the shared expert's weight gradients and its term of dx
+    (the shared expert of the lpnh.cn MoE guide, section 4.10)."""
+    w = SHARED_CASES[name]
+    inp = W.make_inputs(w)
+    sh = inp["shared"]
+    if w.expert_bias:  # nonzero biases everywhere
+        g = torch.Generator().manual_seed(42)
+        for key, shape in (("b1", (w.E, w.H)), ("b2", (w.E, w.d))):
+            inp[key] = (0.1 * torch.randn(*shape, generator=g)).to(w.torch_dtype)
+        sh["b1"] = (0.1 * torch.randn(w.shared_H, generator=g)).to(w.torch_dtype)
+        sh["b2"] = (0.1 * torch.randn(w.d, generator=g)).to(w.torch_dtype)
+    dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(8)).to(w.torch_dtype)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(inp, DEV)
+    ws = moe.workspace_shared(cfg, w.shared_H, DEV)
+    out = moe.layer_forward_shared(cfg, dinp, dinp["shared"], ws=ws)
+    grads, sgrads = moe.layer_backward_shared(cfg, dinp, dinp["shared"], out, dy.to(DEV), 0.05,
+                                              ws=ws)
+    torch.cuda.synchronize()
+    ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, 0.05, w.tau,
+                          logits=out["logits"].cpu().numpy(), shared=sh,
+                          noise_scale=w.noise_scale)
+    np.testing.assert_array_equal(ref["route"]["slot_of"], out["slot_of"].cpu().numpy())
+    errs = {}
+    for key in ("dx", "dWg", "dbias", "dW1", "dW3", "dW2", "db1", "db2"):
+        if ref[key] is not None:
+            errs[key] = rel_err(np_of(grads[key]), ref[key])
+    for key in ("dW1", "dW3", "dW2", "db1", "db2"):
+        if ref["shared"][key] is not None:
+            errs["shared_" + key] = rel_err(np_of(sgrads[key]), ref["shared"][key])
+        else:
+            assert key not in sgrads, key
+    print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    for key, e in errs.items():
+        assert e <= 2e-2, (key, e)
+    assert moe.device_status(ws)[0] == 0
 
 
 def test_backward_is_deterministic():

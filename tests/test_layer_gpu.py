@@ -31,6 +31,10 @@ SMALL = {
     # 16 experts, top-4, Gaussian router noise
     "sweep_small": W.small(WL["sweep_e16_k4"], T=2048, d=256, H=512),
     "sweep_small_single_cta": W.small(WL["sweep_e16_k4"], T=1000, d=128, H=256),
+    # std-scaled router noise (kwkr.cn MoE article, section 3.3)
+    "std_noise_small": W.small(WL["sweep_std_noise"], T=2048, d=256, H=512),
+    # 157 router tiles in two rounds over the 148 CTAs, with drops
+    "tiles_two_rounds": W.small(WL["longtail"], T=20000, d=128, H=64),
 }
 
 
@@ -46,13 +50,21 @@ def test_layer_seeds(seed):
 
 
 FULL = {"ref_fp32": None, "switch_top1": 2048, "decode": None, "longtail": 1024,
-        "mixtral": 128, "sweep_e16_k4": 1024}
+        "mixtral": 128, "sweep_e16_k4": 1024, "sweep_std_noise": 1024}
 
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_layer_full_size(name):
     res = check_layer(WL[name], DEV, n_sample=FULL[name])
     print(name, {k: v for k, v in res.items() if k not in ("out", "r")})
+
+
+@pytest.mark.parametrize("name,seed", [("switch_top1", 1), ("switch_top1", 2),
+                                       ("longtail", 1), ("longtail", 2)])
+def test_layer_full_size_other_seeds(name, seed):
+    """The Switch and long-tail workloads at full size on two more seeds."""
+    res = check_layer(WL[name].with_(seed=seed), DEV, n_sample=512)
+    print(name, seed, {k: v for k, v in res.items() if k not in ("out", "r")})
 
 
 def test_layer_host_io_matches_device_call():

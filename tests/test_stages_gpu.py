@@ -27,6 +27,20 @@ ROUTER_CASES = {
     "E256_k8": W.small(WL["switch_top1"], T=200, d=64, H=64, E=256, k=8, c=Fraction(1)),
     "tau_half": W.small(WL["longtail"], T=90, d=64, H=64).with_(tau=0.5),
     "fp32_E64": W.small(WL["ref_fp32"], T=333, d=96, H=64, E=64, k=3),
+    # 40 tiles on 40 CTAs; 157 tiles on the 148 CTAs (a second round)
+    "tiles_one_round": W.small(WL["longtail"], T=5000, d=128, H=64),
+    "tiles_two_rounds": W.small(WL["sweep_e16_k4"], T=20000, d=64, H=64),
+    # std-scaled router noise (kwkr.cn MoE article, section 3.3) on every
+    # router path: tensor cores (E = 16; E = 64 with a bias), the K-split
+    # decode router, the FMA router (fp32; bf16 with E > 64)
+    "std_noise_E16": W.small(WL["sweep_std_noise"], T=3000, d=256, H=64),
+    "std_noise_E64_bias": W.small(WL["longtail"], T=600, d=128, H=64).with_(
+        noise="gaussian_std", noise_std=0.3),
+    "std_noise_split": WL["decode"].with_(H=64, noise="gaussian_std", noise_std=0.2),
+    "std_noise_fp32": W.small(WL["ref_fp32"], T=300, d=64, H=64, E=12, k=3).with_(
+        noise="gaussian_std", noise_std=0.2),
+    "std_noise_E100": W.small(WL["switch_top1"], T=200, d=64, H=64, E=100, k=2).with_(
+        noise="gaussian_std", noise_std=0.5),
 }
 
 
@@ -39,7 +53,8 @@ def test_router_topk(name):
     lg, idx, gate, psum = moe.router_topk(cfg, d["x"], d["Wg"], d["bias"], d["noise"])
     torch.cuda.synchronize()
     lg = lg.cpu().numpy()
-    ref_l = ORC.router_logits(inp["x"], inp["Wg"], inp["bias"], inp["noise"], w.tau)
+    ref_l = ORC.router_logits(inp["x"], inp["Wg"], inp["bias"], inp["noise"], w.tau,
+                              w.noise_scale)
     assert rel_err(lg, ref_l) <= TOL_LOGITS[w.dtype]
     r = ORC.route_from_logits(lg, w.k, cfg.capacity)
     np.testing.assert_array_equal(idx.cpu().numpy(), r["ids"])

@@ -17,6 +17,19 @@ def test_gaussian_noise_has_the_declared_std():
     assert abs(n.std().item() / w.noise_std - 1.0) < 0.02
 
 
+def test_std_scaled_noise_is_drawn_unscaled():
+    """std-scaled router noise: the tensor is N(0, 1); the router applies the
+    strength noise_std times each token's logit standard deviation."""
+    w = W.WORKLOADS["sweep_std_noise"]
+    inp = W.make_inputs(W.small(w, T=4096, d=64, H=64))
+    n = inp["noise"].double()
+    assert n.shape == (4096, w.E) and inp["noise"].dtype == torch.float32
+    assert abs(n.mean().item()) < 5 / math.sqrt(n.numel())
+    assert abs(n.std().item() - 1.0) < 0.02
+    assert w.noise_scale == w.noise_std > 0
+    assert W.WORKLOADS["sweep_e16_k4"].noise_scale == 0.0
+
+
 def test_gumbel_noise_matches_its_moments():
     w = W.small(W.WORKLOADS["longtail"], T=4096, d=64, H=64)
     n = W.make_inputs(w)["noise"].double()

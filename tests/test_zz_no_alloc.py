@@ -56,6 +56,16 @@ def test_static_scratch_dispatch_matches_workspace_dispatch(T, E, k, c, skew, d)
             assert torch.equal(got[key], ref[key]), key
         assert torch.equal(got["token_of_row"][:R], ref["token_of_row"][:R])
         assert torch.equal(got["xd"][:R], ref["xd"][:R])
+    # after those calls (the first one looked the scratch address up), a
+    # further call changes neither torch's allocations nor the device's free
+    # memory: it allocates nothing
+    got = _empty_outputs(cfg, torch.bfloat16)
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    assert _static_call(cfg, ids, x, got) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_static_scratch_rejects_oversize():
