@@ -36,7 +36,6 @@
 
 #include <math.h>
 #include <mutex>
-#include <type_traits>
 
 namespace moe {
 namespace {
@@ -59,9 +58,12 @@ enum Mode { kPlain = 0, kGelu = 1, kSwiglu = 2, kBwdGelu = 3, kBwdSwiglu = 4 };
 // warp. Four 48 KB stages and two 2 KB buffers per warp fill the 227 KB
 // (measured on B300 against 3 stages + 4 buffers: 1.4 % faster on the
 // switch_top1 FFN, equal on the other workloads, and equal to 4 + 1).
-// EPIW is the number of epilogue warps (8 or 16; a multiple of four, since
-// warp w reads TMEM lanes 32 (w % 4) .. + 31): the CTA has 64 + 32 EPIW
-// threads.
+// EPIW is the number of epilogue warps (a multiple of four, since warp w
+// reads TMEM lanes 32 (w % 4) .. + 31): the CTA has 64 + 32 EPIW threads.
+// Sixteen epilogue warps (four per TMEM lane quarter, 96 registers each,
+// with 4 stages + 1 staging buffer, or 3 + 2) measured on B300 against eight:
+// switch_top1 layer call 2.7 % faster, long tail 0.8 % (3 + 2: 7 %) slower,
+// mixtral equal, so the forward keeps eight.
 template <int STAGES_, int OUT_BUFS_, int EPIW_ = 8>
 struct Pipe {
   static constexpr int STAGES = STAGES_;
@@ -69,28 +71,10 @@ struct Pipe {
   static constexpr int EPIW = EPIW_;
   static constexpr int THREADS = 64 + 32 * EPIW_;
 };
-#ifndef MOE_GEMM_EPIW
-#define MOE_GEMM_EPIW 8
-#endif
-#ifndef MOE_GEMM_STAGES
-#define MOE_GEMM_STAGES 4
-#endif
-#ifndef MOE_GEMM_OUTBUFS
-#define MOE_GEMM_OUTBUFS 2
-#endif
-#ifndef MOE_GEMM_PAIR_STAGES
-#define MOE_GEMM_PAIR_STAGES 6
-#endif
-#ifndef MOE_GEMM_PAIR_OUTBUFS
-#define MOE_GEMM_PAIR_OUTBUFS 2
-#endif
 // forward GEMMs
-using PipeShape = Pipe<MOE_GEMM_STAGES, MOE_GEMM_OUTBUFS, MOE_GEMM_EPIW>;
+using PipeShape = Pipe<4, 2>;
 // A CTA of a pair stages 32 KB per K step, so six stages fit.
-using PipePairShape = Pipe<MOE_GEMM_PAIR_STAGES, MOE_GEMM_PAIR_OUTBUFS, MOE_GEMM_EPIW>;
-// the backward's GEMMs (their epilogue also reads the pre-activations)
-using PipeBwdShape = Pipe<4, 2, 8>;
-using PipeBwdPairShape = Pipe<6, 2, 8>;
+using PipePairShape = Pipe<6, 2>;
 
 template <int STAGES>
 struct SmemTail {
@@ -122,8 +106,6 @@ constexpr size_t smem_bytes() {
 }
 static_assert(smem_bytes<false, PipeShape>() <= 227 * 1024, "shared memory");
 static_assert(smem_bytes<true, PipePairShape>() <= 227 * 1024, "shared memory");
-static_assert(smem_bytes<false, PipeBwdShape>() <= 227 * 1024, "shared memory");
-static_assert(smem_bytes<true, PipeBwdPairShape>() <= 227 * 1024, "shared memory");
 
 // GELU(u) = u/2 (1 + erf(u / sqrt 2)) with erf from the rational
 // approximation of Abramowitz & Stegun, Handbook of Mathematical Functions,
@@ -796,16 +778,13 @@ cudaError_t launch_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                         int32_t* hdr, const int32_t* o_rows, const float* o_scale,
                         cudaStream_t s, const void* pre = nullptr, int ldo = 0, int kb3 = -1) {
   if (!BMN || kb3 < 0) kb3 = (K + BK - 1) / BK;
-  constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu || BMN;
-  using PP = typename std::conditional<BWD, PipeBwdPairShape, PipePairShape>::type;
-  using PS = typename std::conditional<BWD, PipeBwdShape, PipeShape>::type;
   if (pair)
-    return launch_gemm_p<MODE, SCATTER, true, PP, BMN>(a, b, b3, o, offset, E, N, K, bias, out,
-                                                       rows_bound, hdr, o_rows, o_scale, pre, ldo,
-                                                       kb3, s);
-  return launch_gemm_p<MODE, SCATTER, false, PS, BMN>(a, b, b3, o, offset, E, N, K, bias, out,
-                                                      rows_bound, hdr, o_rows, o_scale, pre, ldo,
-                                                      kb3, s);
+    return launch_gemm_p<MODE, SCATTER, true, PipePairShape, BMN>(
+        a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, kb3,
+        s);
+  return launch_gemm_p<MODE, SCATTER, false, PipeShape, BMN>(a, b, b3, o, offset, E, N, K, bias,
+                                                             out, rows_bound, hdr, o_rows,
+                                                             o_scale, pre, ldo, kb3, s);
 }
 
 }  // namespace

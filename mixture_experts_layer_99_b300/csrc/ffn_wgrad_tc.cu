@@ -10,8 +10,10 @@
 // rows starts anywhere (TMA places no alignment rule on the row coordinate);
 // the last block of an expert also holds rows of the next expert, so a
 // fix-up warp zeroes those rows of the A tile in shared memory before the
-// MMA reads it (and of the B tile too after the last expert's rows, where the
-// buffers hold no data: 0 x NaN would not vanish).
+// MMA reads it (and of the B tile too whenever the block reaches past the
+// last kept row, where the buffers hold no data: 0 x NaN would not vanish;
+// that is the last expert's block, and an earlier expert's when the experts
+// after it hold fewer rows than the block's padding).
 //
 // Kernel layout as in the grouped GEMM (one CTA per SM, warp 0 TMA producer,
 // warp 1 MMA issuer, warps 2-9 epilogue, warp 10 the fix-up, two 256-column
@@ -58,11 +60,13 @@ constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(Smem)
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // tile -> expert, first m and n, first row of the expert, its K blocks, the
-// rows of its last block that belong to it (1..64), and whether its rows end
-// where all rows end
+// rows of its last block that belong to it (1..64), and whether that block
+// reaches past the end of all rows (off[E]: rows no one wrote). The last
+// block of any expert can: of the last one, and of an earlier one when the
+// experts after it hold fewer rows than the block's padding.
 struct WTile {
   int e, m0, n0, row0, nkb, tail;
-  bool at_end;
+  bool past_end;
 };
 __device__ __forceinline__ WTile wtile(const int32_t* __restrict__ off, int E, int mtc, int ntc,
                                        int tile) {
@@ -76,7 +80,7 @@ __device__ __forceinline__ WTile wtile(const int32_t* __restrict__ off, int E, i
   const int rows = __ldg(off + w.e + 1) - w.row0;
   w.nkb = rows > 0 ? (rows + BK - 1) / BK : 0;
   w.tail = rows - (w.nkb - 1) * BK;
-  w.at_end = w.row0 + rows == __ldg(off + E);
+  w.past_end = w.row0 + w.nkb * BK > __ldg(off + E);
   return w;
 }
 
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *reinterpret_cast<uint4*>(a + box * BOX_BYTES + (w.tail + (j >> 3)) * 128 +
                                       (j & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
-          if (w.at_end) {
+          if (w.past_end) {
             uint8_t* b = sB + stage * B_BYTES;
             for (int i = lane; i < (UMMA_N / 64) * nz; i += 32) {
               const int box = i / nz, j = i - box * nz;

@@ -106,10 +106,20 @@ def test_backward_shared_expert_matches_oracle(name):
     cfg = moe.config_from_workload(w)
     dinp = W.to_device(inp, DEV)
     ws = moe.workspace_shared(cfg, w.shared_H, DEV)
+    bws = moe.workspace_backward_shared(cfg, w.shared_H, DEV)
+    ws[256:].fill_(255)    # NaN bytes: nothing may read what no kernel wrote
+    bws[256:].fill_(255)
     out = moe.layer_forward_shared(cfg, dinp, dinp["shared"], ws=ws)
     grads, sgrads = moe.layer_backward_shared(cfg, dinp, dinp["shared"], out, dy.to(DEV), 0.05,
-                                              ws=ws)
+                                              ws=ws, bws=bws)
     torch.cuda.synchronize()
+    assert moe.device_status(bws)[0] == 0
+    for key, t in grads.items():
+        bad = torch.isnan(t)
+        if bad.any():
+            idx = torch.nonzero(bad)[:8].tolist()
+            raise AssertionError(f"{key}: {int(bad.sum())} NaN, first at {idx}; "
+                                 f"offsets {out['expert_offset'].tolist()}")
     ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, 0.05, w.tau,
                           logits=out["logits"].cpu().numpy(), shared=sh,
                           noise_scale=w.noise_scale)
@@ -127,6 +137,35 @@ def test_backward_shared_expert_matches_oracle(name):
     for key, e in errs.items():
         assert e <= 2e-2, (key, e)
     assert moe.device_status(ws)[0] == 0
+
+
+@pytest.mark.parametrize("name", ["longtail_small", "drops_heavy", "switch_small"])
+def test_backward_reads_no_unwritten_workspace_bytes(name):
+    """Both workspaces start filled with NaN bytes (past their status
+    headers): the forward and the backward must read only what they wrote, so
+    the gradients still match the oracle. (The last 64-row block of an expert
+    that is not the last one can reach past the final kept row; its unwritten
+    rows must be zeroed before the weight-gradient product reads them.)"""
+    w, alpha, with_bias = CASES[name]
+    inp = W.make_inputs(w)
+    dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(11)).to(w.torch_dtype)
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(inp, DEV)
+    ws = moe.workspace(cfg, DEV)
+    bws = moe.workspace_backward(cfg, DEV)
+    ws[256:].fill_(255)
+    bws[256:].fill_(255)
+    out = moe.layer_forward(cfg, dinp, ws=ws)
+    grads = moe.layer_backward(cfg, dinp, out, dy.to(DEV), alpha, ws=ws, bws=bws)
+    torch.cuda.synchronize()
+    assert moe.device_status(bws)[0] == 0
+    ref = OB.moe_backward(inp, w.k, w.c, w.act, dy, alpha, w.tau,
+                          logits=out["logits"].cpu().numpy())
+    for key in ("dx", "dWg", "dbias", "dW1", "dW3", "dW2"):
+        if ref[key] is None:
+            continue
+        assert not torch.isnan(grads[key]).any(), key
+        assert rel_err(np_of(grads[key]), ref[key]) <= TOL[key], key
 
 
 def test_backward_is_deterministic():

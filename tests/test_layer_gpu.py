@@ -67,6 +67,26 @@ def test_layer_full_size_other_seeds(name, seed):
     print(name, seed, {k: v for k, v in res.items() if k not in ("out", "r")})
 
 
+@pytest.mark.parametrize("name", ["ref_fp32", "switch_small", "mixtral_small",
+                                  "longtail_small", "drops_heavy", "sweep_small"])
+def test_layer_reads_no_unwritten_workspace_bytes(name):
+    """A workspace filled with NaN bytes (past its status header) gives the
+    same outputs, bit for bit, as a zeroed one: the layer reads only what it
+    wrote in the same call."""
+    w = SMALL[name]
+    cfg = moe.config_from_workload(w)
+    dinp = W.to_device(W.make_inputs(w), DEV)
+    outs = []
+    for fill in (0, 255):
+        ws = moe.workspace(cfg, DEV)
+        ws[256:].fill_(fill)
+        outs.append(moe.layer_forward(cfg, dinp, ws=ws))
+        torch.cuda.synchronize()
+        assert moe.device_status(ws)[0] == 0
+    for key, t in outs[0].items():
+        assert torch.equal(t, outs[1][key]), key
+
+
 def test_layer_host_io_matches_device_call():
     w = W.small(WL["switch_top1"], T=512, d=128, H=256)
     cfg = moe.config_from_workload(w)
