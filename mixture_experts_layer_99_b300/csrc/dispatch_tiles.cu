@@ -1,5 +1,8 @@
 // Dispatch and load-balance statistics fed by the tensor-core router, in one
 // kernel with one block per router tile (at most 128 tokens, a multiple of 8).
+// The statistics are summed in fp32 in fixed orders (pairwise trees and
+// butterflies): B300's fp64 rate is a small fraction of its fp32 rate, and
+// the fp64 form of these sums kept the kernel's block 0 busy for about 10 us.
 //
 // The router already counted, for every tile, how many of the tile's slots
 // chose each expert, and summed p per expert per CTA. From those each block
@@ -16,7 +19,7 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     int y_vec16) {
   __shared__ int tot[kMaxE], base[kMaxE], offs[kMaxE + 1];
   __shared__ int wcnt[8][kMaxE];
-  __shared__ double psum[kMaxE];
+  __shared__ float psum[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int tile = blockIdx.x;
   for (int i = tid; i < 8 * kMaxE; i += 256) (&wcnt[0][0])[i] = 0;
@@ -144,34 +147,50 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     if (lane == 0) offs[E] = run;
   }
   if (tile == 0) {
-    // probability sums per expert: lane-strided partials, fixed butterfly
-    for (int e = w; e < E; e += 8) {
-      double sp = 0.0;
-      for (int b = lane; b < nparts; b += 32) sp += (double)partial[(size_t)b * E + e];
-      sp = warp_sum_d(sp);
-      if (lane == 0) psum[e] = sp;
+    // probability sums per expert: R neighbouring threads per expert (R as
+    // above), thread sub adding partials sub, sub + R, ... in that order (the
+    // loads of every expert in flight together, eight per round), then a fixed
+    // butterfly over the R threads
+    int R = 32;
+    while (R * E > 256) R >>= 1;
+    const int e = tid / R, sub = tid % R;
+    float sp = 0.f;
+    if (e < E) {
+      for (int b0 = sub; b0 < nparts; b0 += 8 * R) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int b = b0 + i * R;
+          v[i] = b < nparts ? __ldg(partial + (size_t)b * E + e) : 0.f;
+        }
+        // the eight as a pairwise tree, then into the running sum
+        sp += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+      }
     }
+    for (int o = 1; o < R; o <<= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    if (e < E && sub == 0) psum[e] = sp;
   }
   __syncthreads();
   if (tile == 0) {
     for (int e = tid; e <= E; e += 256) offset[e] = offs[e];
     if (w == 0) {
-      double fp = 0.0;
+      const float kT = (float)((long long)k * T), fT = (float)T;
+      float fp = 0.f;
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
         if (e < E) {
           count[e] = tot[e];
-          const double fe = (double)tot[e] / ((double)k * (double)T);
-          const double Pe = psum[e] / (double)T;
-          if (f) f[e] = (float)fe;
-          if (P) P[e] = (float)Pe;
-          if (prob_sum) prob_sum[e] = (float)psum[e];
-          fp += fe * Pe;
+          const float fe = (float)tot[e] / kT;
+          const float Pe = psum[e] / fT;
+          if (f) f[e] = fe;
+          if (P) P[e] = Pe;
+          if (prob_sum) prob_sum[e] = psum[e];
+          fp = fmaf(fe, Pe, fp);
         }
       }
-      fp = warp_sum_d(fp);
+      fp = warp_sum_f(fp);
       if (lane == 0) {
-        if (Lb) Lb[0] = (float)((double)E * fp);
+        if (Lb) Lb[0] = (float)E * fp;
         if (dropped) dropped[0] = (int32_t)((long long)k * T - offs[E]);
       }
     }
