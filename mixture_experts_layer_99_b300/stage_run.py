@@ -3,7 +3,10 @@ given number of times: a bounded program for a profiler to capture one kernel
 of (``ncu -k regex:<kernel> ...``). It times nothing and checks nothing.
 
     python -m mixture_experts_layer_99_b300.stage_run --workload mixtral \
-        [--E 2] [--T 4096] [--stage layer|router|dispatch|ffn|combine] [--calls 4]
+        [--E 2] [--T 4096] [--stage layer|router|dispatch|ffn|combine|backward] [--calls 4]
+
+``backward`` runs moe_layer_backward (loss sum <dy, y> + 0.01 L_balance, dy
+seeded) after the layer call it differentiates.
 
 ``--E`` / ``--T`` shrink the workload (a workload without drops, c = E/k,
 keeps c = E'/k so that it still drops nothing); with the same T, d and k the
@@ -39,7 +42,7 @@ def main():
     ap.add_argument("--E", type=int, default=None)
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--stage", default="layer",
-                    choices=["layer", "router", "dispatch", "ffn", "combine"])
+                    choices=["layer", "router", "dispatch", "ffn", "combine", "backward"])
     ap.add_argument("--calls", type=int, default=4)
     args = ap.parse_args()
     w = reduced(W.WORKLOADS[args.workload], args.E, args.T)
@@ -56,6 +59,11 @@ def main():
         Y = moe.expert_ffn(cfg, d["xd"], d["offset"], inp["W1"], inp["W2"], inp.get("W3"),
                            inp.get("b1"), inp.get("b2"), ws=ws)
         torch.cuda.synchronize(dev)
+    if args.stage == "backward":
+        dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(5)).to(
+            w.torch_dtype).to(dev)
+        bws = moe.workspace_backward(cfg, dev)
+        grads = moe.alloc_grads(cfg, inp, dev)
     for _ in range(args.calls):
         if args.stage == "layer":
             moe.layer_forward(cfg, inp, ws=ws, out=out)
@@ -66,8 +74,10 @@ def main():
         elif args.stage == "ffn":
             moe.expert_ffn(cfg, d["xd"], d["offset"], inp["W1"], inp["W2"], inp.get("W3"),
                            inp.get("b1"), inp.get("b2"), ws=ws, Y=Y)
-        else:
+        elif args.stage == "combine":
             moe.combine(cfg, Y, d["slot_of"], out["topk_gate"])
+        else:
+            moe.layer_backward(cfg, inp, out, dy, 0.01, ws=ws, bws=bws, grads=grads)
     torch.cuda.synchronize(dev)
     print(f"stage_run: {w.name} {args.stage} x{args.calls}, status {moe.device_status(ws)}")
 
