@@ -41,8 +41,11 @@
  *     intermediates and a status header. Zero it once with moe_workspace_init
  *     before first use; afterwards calls leave the header ready for the next
  *     call. Calls sharing one workspace must be ordered (same stream).
- *   - Device-detected errors (a bounded wait that ran out) are recorded in the
- *     workspace header and read with moe_device_status.
+ *   - Device-detected errors are recorded in the workspace header and read
+ *     with moe_device_status: a bounded wait that ran out
+ *     (MOE_ERR_DEVICE_TIMEOUT), or a device-resident input of moe_dispatch or
+ *     moe_expert_ffn out of range (MOE_ERR_INVALID_ARG; the host cannot check
+ *     those without a synchronisation).
  *   - Limits: 1 <= k <= 8, k <= E <= 256, T >= 1, T*k < 2^31, capacity >= 1;
  *     d and H multiples of 8 (bf16) or 4 (fp32); activations must be finite.
  */
@@ -116,8 +119,12 @@ MOE_API moe_status_t moe_workspace_size(const moe_config_t *cfg, size_t *bytes);
 MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Read and clear the device status word in ws. Synchronises `stream`.
- * *code is MOE_OK, or the status a kernel recorded (MOE_ERR_DEVICE_TIMEOUT).
- * *where identifies the waiting kernel role (0 if none). */
+ * *code is MOE_OK, or the first status a kernel recorded since the last read
+ * (MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_INVALID_ARG). *where says which kernel
+ * recorded it (0 if none): 1..6 a wait of the grouped GEMM (roles: producer,
+ * MMA issuer, epilogue), 41 an expert id outside [0, E) in moe_dispatch, 42 /
+ * 43 bad expert offsets in moe_expert_ffn (bf16 / fp32 kernel), 11..14 a
+ * wait of the tensor-core router, 21..27 a wait of the weight-gradient GEMM. */
 MOE_API moe_status_t moe_device_status(void *ws, int32_t *code, int32_t *where,
                                moe_stream_t stream);
 
@@ -147,7 +154,10 @@ MOE_API moe_status_t moe_router_topk(const moe_config_t *cfg, const void *x, con
  *   token_of_row  [T*k]    int32 out: token of each packed row; the first
  *                          expert_offset[E] entries are written
  *   xd            [T*k, d] out (dtype): xd[slot_of[t,j]] = x[t]; first
- *                          expert_offset[E] rows written */
+ *                          expert_offset[E] rows written
+ * An id outside [0, E) in topk_idx is counted for no expert, its slot gets
+ * slot_of = -1, the other slots are dispatched as if it were absent, and the
+ * workspace header records MOE_ERR_INVALID_ARG (where = 41). */
 MOE_API moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const void *x,
                           int32_t *expert_count, int32_t *expert_offset, int32_t *slot_of,
                           int32_t *token_of_row, void *xd, void *ws, size_t ws_bytes,
@@ -168,7 +178,9 @@ MOE_API moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_i
  *   All calls share the one array: calls that overlap on the GPU (different
  *   streams, or several host threads) race and corrupt each other's results;
  *   order them on one stream. Each call rewrites all the scratch it reads, so
- *   leftovers of earlier calls never matter. */
+ *   leftovers of earlier calls never matter.
+ *   An id outside [0, E) is left out as in moe_dispatch but, with no
+ *   workspace header, not reported. */
 MOE_API moe_status_t moe_dispatch_static_scratch(const moe_config_t *cfg, const int32_t *topk_idx,
                                                  const void *x, int32_t *expert_count,
                                                  int32_t *expert_offset, int32_t *slot_of,
@@ -184,7 +196,11 @@ MOE_API moe_status_t moe_dispatch_static_scratch(const moe_config_t *cfg, const 
  *   Y             [T*k, d] out (dtype), first expert_offset[E] rows written.
  * bf16 runs on the tcgen05 tensor cores with fp32 accumulation; the hidden
  * activation h is rounded to bf16 between the two GEMMs. fp32 runs on fp32
- * FMA. */
+ * FMA.
+ * The offsets must satisfy expert_offset[0] = 0 <= expert_offset[1] <= ... <=
+ * expert_offset[E] <= min(T*k, E*C); otherwise no row is computed (Y is left
+ * as it was) and the workspace header records MOE_ERR_INVALID_ARG (where = 42
+ * for bf16, 43 for fp32). */
 MOE_API moe_status_t moe_expert_ffn(const moe_config_t *cfg, const void *xd,
                             const int32_t *expert_offset, const void *W1, const void *W3,
                             const void *W2, const void *b1, const void *b2, void *Y,

@@ -91,7 +91,7 @@ cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* off
                        cudaStream_t s) {
   if (c.dtype == MOE_BF16)
     return launch_ffn_tc(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, hdr, s);
-  return launch_ffn_simt(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, s);
+  return launch_ffn_simt(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, hdr, s);
 }
 
 }  // namespace moe
@@ -225,7 +225,8 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* topk_idx, cons
   return cuda_status(launch_dispatch(*cfg, topk_idx, x, expert_count, expert_offset, slot_of,
                                      token_of_row, xd, at<int32_t>(ws, L.disp_hist),
                                      at<int32_t>(ws, L.disp_base),
-                                     (int64_t)cfg->T * cfg->k, (cudaStream_t)stream));
+                                     (int64_t)cfg->T * cfg->k, (cudaStream_t)stream,
+                                     at<int32_t>(ws, L.hdr)));
 }
 
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* xd,

@@ -18,21 +18,29 @@ constexpr int NT = 256;
 constexpr int NW = NT / 32;
 constexpr int SPW = SPB / NW;  // slots per warp (128)
 
-// hist[b, e] = number of slots of block b that chose expert e.
+// hist[b, e] = number of slots of block b that chose expert e. An expert
+// id outside [0, E) (a caller's input) counts for no expert, its slot gets
+// row -1, and with a status header it is recorded as MOE_ERR_INVALID_ARG
+// (where = 41).
 __global__ void __launch_bounds__(NT) disp_count_kernel(const int32_t* __restrict__ idx,
                                                         int64_t nslots, int E,
-                                                        int32_t* __restrict__ hist) {
+                                                        int32_t* __restrict__ hist,
+                                                        int32_t* __restrict__ hdr) {
   __shared__ int h[kMaxE];
   for (int e = threadIdx.x; e < E; e += NT) h[e] = 0;
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * SPB;
+  bool bad = false;
   for (int i = threadIdx.x; i < SPB; i += NT) {
     const int64_t s = s0 + i;
     if (s < nslots) {
       const int e = idx[s];
       if ((unsigned)e < (unsigned)E) atomicAdd(&h[e], 1);
+      else bad = true;
     }
   }
+  if (bad && hdr != nullptr && atomicCAS(hdr + kHdrStatus, 0, (int)MOE_ERR_INVALID_ARG) == 0)
+    atomicExch(hdr + kHdrWhere, 41);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += NT) hist[(size_t)blockIdx.x * E + e] = h[e];
 }
@@ -168,10 +176,10 @@ cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* t
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,
                             int32_t* count, int32_t* offset, int32_t* slot_of,
                             int32_t* token_of_row, void* xd, int32_t* hist, int32_t* base,
-                            int64_t rows_bound, cudaStream_t s) {
+                            int64_t rows_bound, cudaStream_t s, int32_t* hdr) {
   const int64_t nslots = (int64_t)c.T * c.k;
   const int nblk = disp_blocks(c);
-  disp_count_kernel<<<nblk, NT, 0, s>>>(idx, nslots, c.E, hist);
+  disp_count_kernel<<<nblk, NT, 0, s>>>(idx, nslots, c.E, hist, hdr);
   disp_scan_kernel<<<1, 1024, 0, s>>>(hist, nblk, c.E, c.capacity, base, count, offset);
   disp_assign_kernel<<<nblk, NT, 0, s>>>(idx, nslots, c.k, c.E, c.capacity, base, offset,
                                          slot_of, token_of_row);

@@ -35,9 +35,20 @@ __device__ __forceinline__ float gelu_erf(float u) {
 __device__ __forceinline__ float silu_f(float u) { return u / (1.f + expf(-u)); }
 
 // Finds (expert, first row, end row) of linear m-tile `tile`; returns false if
-// the tile is beyond the last expert's rows.
-__device__ bool find_tile(const int32_t* offset, int E, int tile, int bm, int* e_out,
-                          int* m0_out, int* mend_out) {
+// the tile is beyond the last expert's rows. The offsets may be a caller's
+// input (moe_expert_ffn): unless offset[0] = 0 <= offset[1] <= ... <=
+// offset[E] <= rows_limit, no tile runs and the status header records
+// MOE_ERR_INVALID_ARG (where = 43).
+__device__ bool find_tile(const int32_t* offset, int E, int rows_limit, int32_t* hdr, int tile,
+                          int bm, int* e_out, int* m0_out, int* mend_out) {
+  bool bad = offset[0] != 0;
+  for (int e = 0; e < E; ++e) bad |= offset[e + 1] < offset[e];
+  bad |= offset[E] > rows_limit;
+  if (bad) {
+    if (hdr != nullptr && atomicCAS(hdr + kHdrStatus, 0, (int)MOE_ERR_INVALID_ARG) == 0)
+      atomicExch(hdr + kHdrWhere, 43);
+    return false;
+  }
   int cum = 0;
   for (int e = 0; e < E; ++e) {
     const int r0 = offset[e], r1 = offset[e + 1];
@@ -60,7 +71,8 @@ __global__ void __launch_bounds__(NT) ffn_simt_kernel(const T* __restrict__ A,
                                                       const T* __restrict__ bias,
                                                       T* __restrict__ Cout,
                                                       const int32_t* __restrict__ offset, int E,
-                                                      int N, int K) {
+                                                      int N, int K, int rows_limit,
+                                                      int32_t* __restrict__ hdr) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   __shared__ float B3s[EPI == kEpiSwiglu ? BK : 1][BN + 4];
@@ -68,7 +80,7 @@ __global__ void __launch_bounds__(NT) ffn_simt_kernel(const T* __restrict__ A,
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   if (tid == 0) {
     int e = -1, m0 = 0, mend = 0;
-    if (!find_tile(offset, E, blockIdx.y, BM, &e, &m0, &mend)) e = -1;
+    if (!find_tile(offset, E, rows_limit, hdr, blockIdx.y, BM, &e, &m0, &mend)) e = -1;
     s_e = e;
     s_m0 = m0;
     s_mend = mend;
@@ -141,23 +153,24 @@ template <typename T>
 cudaError_t launch_ffn_simt_t(const moe_config_t& c, const void* xd, const int32_t* offset,
                               const void* W1, const void* W3, const void* W2,
                               const void* b1, const void* b2, void* Y, void* h,
-                              int64_t rows_bound, cudaStream_t s) {
+                              int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
   const int64_t mt = (rows_bound + BM - 1) / BM + c.E;
+  const int rl = (int)(rows_bound < INT32_MAX ? rows_bound : INT32_MAX);
   dim3 g1((c.H + BN - 1) / BN, (unsigned)mt), g2((c.d + BN - 1) / BN, (unsigned)mt);
   const T* A = static_cast<const T*>(xd);
   T* hp = static_cast<T*>(h);
   if (c.act == MOE_ACT_SWIGLU)
     ffn_simt_kernel<T, kEpiSwiglu><<<g1, NT, 0, s>>>(A, static_cast<const T*>(W1),
                                                      static_cast<const T*>(W3), nullptr, hp,
-                                                     offset, c.E, c.H, c.d);
+                                                     offset, c.E, c.H, c.d, rl, hdr);
   else
     ffn_simt_kernel<T, kEpiGelu><<<g1, NT, 0, s>>>(A, static_cast<const T*>(W1), nullptr,
                                                    static_cast<const T*>(b1), hp, offset,
-                                                   c.E, c.H, c.d);
+                                                   c.E, c.H, c.d, rl, hdr);
   ffn_simt_kernel<T, kEpiNone><<<g2, NT, 0, s>>>(
       hp, static_cast<const T*>(W2), nullptr,
       c.act == MOE_ACT_GELU ? static_cast<const T*>(b2) : nullptr, static_cast<T*>(Y),
-      offset, c.E, c.d, c.H);
+      offset, c.E, c.d, c.H, rl, hdr);
   return cudaGetLastError();
 }
 
@@ -166,11 +179,11 @@ cudaError_t launch_ffn_simt_t(const moe_config_t& c, const void* xd, const int32
 cudaError_t launch_ffn_simt(const moe_config_t& c, const void* xd, const int32_t* offset,
                             const void* W1, const void* W3, const void* W2, const void* b1,
                             const void* b2, void* Y, void* h, int64_t rows_bound,
-                            cudaStream_t s) {
+                            int32_t* hdr, cudaStream_t s) {
   if (c.dtype == MOE_F32)
-    return launch_ffn_simt_t<float>(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, s);
+    return launch_ffn_simt_t<float>(c, xd, offset, W1, W3, W2, b1, b2, Y, h, rows_bound, hdr, s);
   return launch_ffn_simt_t<__nv_bfloat16>(c, xd, offset, W1, W3, W2, b1, b2, Y, h,
-                                          rows_bound, s);
+                                          rows_bound, hdr, s);
 }
 
 }  // namespace moe

@@ -219,7 +219,8 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
                            __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
                            const int32_t* __restrict__ o_rows,
                            const float* __restrict__ o_scale,
-                           const __nv_bfloat16* __restrict__ pre, int ldo, int kb3) {
+                           const __nv_bfloat16* __restrict__ pre, int ldo, int kb3,
+                           int rows_limit) {
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
   constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu;
   constexpr int STAGES = PIPE::STAGES;
@@ -274,10 +275,20 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
   pdl_wait();
   const int n_tiles_n = (N + BN_OUT - 1) / BN_OUT;
   if (warp == 2) {  // tbase[e] = sum_{e'<e} m-tiles(e') * n_tiles_n
+    // The offsets may be a caller's input (moe_expert_ffn): unless offset[0]
+    // = 0 <= offset[1] <= ... <= offset[E] <= rows_limit, no tile runs (a
+    // negative row would start a TMA store before the tensor) and the status
+    // header records MOE_ERR_INVALID_ARG (where = 42).
     int run = 0;
+    bool bad = false;
     for (int e0 = 0; e0 <= E; e0 += 32) {
       const int e = e0 + lane;
-      const int mt = e < E ? (__ldg(offset + e + 1) - __ldg(offset + e) + BM_T - 1) / BM_T : 0;
+      int mt = 0;
+      if (e < E) {
+        const int lo = __ldg(offset + e), hi = __ldg(offset + e + 1);
+        bad |= hi < lo || hi > rows_limit || (e == 0 && lo != 0);
+        mt = bad ? 0 : (hi - lo + BM_T - 1) / BM_T;
+      }
       int incl = mt * n_tiles_n;
       const int v = incl;
 #pragma unroll
@@ -288,7 +299,12 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
       if (e <= E) st.tbase[e] = run + incl - v;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) st.n_tiles_total = st.tbase[E];
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      st.n_tiles_total = bad ? 0 : st.tbase[E];
+      if (bad && hdr != nullptr && atomicCAS(hdr, 0, (int)MOE_ERR_INVALID_ARG) == 0)
+        atomicExch(hdr + 1, 42);
+    }
   }
   tc_fence_before();
   if (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote signal
@@ -767,7 +783,8 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   return launch_pdl_cluster(kernel, dim3(grid), dim3(PIPE::THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
                             b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
                             static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale,
-                            static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N, kb3);
+                            static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N, kb3,
+                            (int)(rows_bound < INT32_MAX ? rows_bound : INT32_MAX));
 }
 
 // BMN (B MN-major): kb3 is the first K block read through b3 (< 0: none).

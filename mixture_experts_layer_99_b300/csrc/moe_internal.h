@@ -181,7 +181,7 @@ cudaError_t launch_prob_reduce(const moe_config_t& c, const float* partial, int 
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,
                             int32_t* count, int32_t* offset, int32_t* slot_of,
                             int32_t* token_of_row, void* xd, int32_t* hist, int32_t* base,
-                            int64_t rows_bound, cudaStream_t s);
+                            int64_t rows_bound, cudaStream_t s, int32_t* hdr = nullptr);
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* token_of_row,
                           const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s);
 cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* idx,
@@ -197,7 +197,7 @@ cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* off
 cudaError_t launch_ffn_simt(const moe_config_t& c, const void* xd, const int32_t* offset,
                             const void* W1, const void* W3, const void* W2, const void* b1,
                             const void* b2, void* Y, void* h, int64_t rows_bound,
-                            cudaStream_t s);
+                            int32_t* hdr, cudaStream_t s);
 // Fusion of the tensor-core FFN inside the fused layer call: for k = 1 GEMM2
 // writes gate * row straight to y[token] (no Y buffer, no combine).
 struct FfnFusion {

@@ -272,3 +272,73 @@ def test_tensor_core_activation_accuracy(act):
     bound = 0.5 * _bf16_ulp(exact) + 4e-6 * np.abs(exact) + 3e-7 * np.maximum(1.0, np.abs(u))
     bad = np.abs(y - exact) > bound
     assert not bad.any(), (u[bad][:5], y[bad][:5], exact[bad][:5])
+
+
+# ---------------------------------------------------------------------------
+# device-resident inputs out of range: recorded in the workspace header, the
+# rest of the call unaffected (ids) or nothing computed (offsets)
+# ---------------------------------------------------------------------------
+BAD_IDS = [-1, 1 << 30, -(1 << 31)]
+
+
+@pytest.mark.parametrize("T,E,k,c,dt", [(1000, 16, 2, Fraction(1, 2), "bf16"),
+                                        (257, 5, 3, Fraction(1), "f32")])
+def test_dispatch_out_of_range_ids_are_left_out_and_reported(T, E, k, c, dt):
+    ids = W.make_routing(T, E, k, seed=11, skew=1.0)
+    g = torch.Generator().manual_seed(12)
+    bad = torch.rand(T, k, generator=g) < 0.1
+    vals = torch.tensor(BAD_IDS + [E, E + 3], dtype=torch.int32)
+    ids_bad = torch.where(bad, vals[torch.randint(len(vals), (T, k), generator=g)], ids)
+    x = W.make_rows(T, 32, torch.float32 if dt == "f32" else torch.bfloat16, seed=2)
+    C = ORC.capacity(c, k, T, E)
+    cfg = moe.make_config(T, 32, E, k, 8, C, dt, "gelu")
+    ws = moe.workspace(cfg, DEV)
+    out = moe.dispatch(cfg, ids_bad.to(DEV), x.to(DEV), ws=ws)
+    assert moe.device_status(ws) == (1, 41)    # MOE_ERR_INVALID_ARG, the dispatch count
+    # expected: every bad id as a choice of an extra last expert E, then
+    # that expert removed (offsets of the first E experts are unchanged)
+    r = ORC.dispatch(torch.where(bad, E, ids).numpy(), E + 1, C)
+    np.testing.assert_array_equal(out["count"].cpu().numpy(), r["count"][:E])
+    np.testing.assert_array_equal(out["offset"].cpu().numpy(), r["offset"][:E + 1])
+    np.testing.assert_array_equal(out["slot_of"].cpu().numpy(),
+                                  np.where(bad.numpy(), -1, r["slot_of"]))
+    R = int(r["offset"][E])
+    np.testing.assert_array_equal(out["token_of_row"][:R].cpu().numpy(), r["token_of_row"][:R])
+    assert torch.equal(out["xd"][:R].cpu(), x[torch.from_numpy(r["token_of_row"][:R]).long()])
+    # the status was cleared by the read; a valid call leaves it clean
+    moe.dispatch(cfg, ids.to(DEV), x.to(DEV), ws=ws)
+    assert moe.device_status(ws) == (0, 0)
+
+
+def _bad_offsets(E, R):
+    ok = np.linspace(0, R, E + 1).astype(np.int32)
+    cases = {}
+    o = ok.copy(); o[0] = 3; cases["first_not_zero"] = o
+    o = ok.copy(); o[1], o[2] = o[2], o[1]; cases["decreasing"] = o
+    o = ok.copy(); o[1] = -256; cases["negative"] = o
+    o = ok.copy(); o[E] = R + 1; cases["past_rows"] = o
+    o = ok.copy(); o[1:] = 2 ** 31 - 1; cases["huge"] = o
+    return ok, cases
+
+
+@pytest.mark.parametrize("E,d,H,act,dt,rows", [(3, 64, 128, "gelu", "bf16", 600),
+                                                (2, 256, 256, "swiglu", "bf16", 2100),
+                                                (3, 64, 128, "swiglu", "f32", 300)])
+def test_expert_ffn_bad_offsets_compute_nothing_and_report(E, d, H, act, dt, rows):
+    w, inp, _ = _ffn_case(E, d, H, act, dt, [rows // E] * (E - 1) + [rows - rows // E * (E - 1)],
+                          seed=5)
+    cfg = moe.make_config(rows, d, E, 1, H, rows, dt, act)     # rows bound: T k = rows
+    dv = W.to_device(inp, DEV)
+    ws = moe.workspace(cfg, DEV)
+    ok, cases = _bad_offsets(E, rows)
+    where = 43 if dt == "f32" else 42
+    for name, o in cases.items():
+        Y = torch.full((rows, d), 7.0, dtype=dv["x"].dtype, device=DEV)
+        moe.expert_ffn(cfg, dv["x"], torch.from_numpy(o).to(DEV), dv["W1"], dv["W2"], dv["W3"],
+                       dv["b1"], dv["b2"], ws=ws, Y=Y)
+        assert moe.device_status(ws) == (1, where), name
+        assert bool((Y == 7.0).all()), name
+    Y = moe.expert_ffn(cfg, dv["x"], torch.from_numpy(ok).to(DEV), dv["W1"], dv["W2"], dv["W3"],
+                       dv["b1"], dv["b2"], ws=ws)
+    assert moe.device_status(ws) == (0, 0)
+    assert bool(torch.isfinite(Y.float()).all())
