@@ -498,7 +498,7 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   L.total = off;
   return L;
 }
-bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 && router_tc_supported(c); }
+bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16; }
 
 // The shared expert's part of the backward workspace, after the routed part:
 // its recomputed pre-activations and activation gradients [T, Hps], its dx

@@ -150,6 +150,83 @@ __global__ void __launch_bounds__(128) bwd_router_kernel(
   }
 }
 
+// The same for E > 64: one warp per token, expert e = 32 i + lane in slot i
+// of its lane (EPL = experts per lane), the sums over experts by warp
+// butterflies in a fixed order.
+__device__ __forceinline__ float warp_sum_bwd(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int EPL>
+__global__ void __launch_bounds__(NT) bwd_router_wide_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ idx,
+    const float* __restrict__ gate, const float* __restrict__ dg,
+    const float* __restrict__ f, float alpha, float tau, int T, int E, int k,
+    float* __restrict__ dz, __nv_bfloat16* __restrict__ dzb, int Kp) {
+  const int t = blockIdx.x * NW + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  float p[EPL], dp[EPL];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = 32 * i + lane;
+    p[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    m = fmaxf(m, p[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    p[i] = 32 * i + lane < E ? expf(p[i] - m) : 0.f;
+    s += p[i];
+  }
+  const float inv_s = 1.f / warp_sum_bwd(s);
+  const float bal = alpha * (float)E / (float)T;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = 32 * i + lane;
+    p[i] *= inv_s;
+    dp[i] = e < E ? bal * f[e] : 0.f;
+  }
+  // S = sum_j p[K_j], gdg = sum_j g_j dg_j (the same in every lane)
+  float S = 0.f, gdg = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(size_t)t * k + j];
+    float mine = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (i == (e >> 5)) mine = p[i];
+    S += __shfl_sync(0xffffffffu, mine, e & 31);
+    gdg = fmaf(gate[(size_t)t * k + j], dg[(size_t)t * k + j], gdg);
+  }
+  const float inv_S = 1.f / S;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(size_t)t * k + j];
+    const float add = (dg[(size_t)t * k + j] - gdg) * inv_S;
+    if ((e & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (i == (e >> 5)) dp[i] += add;
+    }
+  }
+  float pdp = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) pdp = fmaf(p[i], dp[i], pdp);
+  pdp = warp_sum_bwd(pdp);
+  const float inv_tau = 1.f / tau;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = 32 * i + lane;
+    const float z = e < E ? p[i] * (dp[i] - pdp) * inv_tau : 0.f;
+    if (e < E) dz[(size_t)t * E + e] = z;
+    // bf16 copy with the experts padded to Kp (zeros past E)
+    if (e < Kp) dzb[(size_t)t * Kp + e] = __float2bfloat16_rn(z);
+  }
+}
+
 // dx_t = sum over the kept slots of dxd[slot] (slot order) + dxr_t (the
 // router term dz_t W_g from the tensor cores) [+ dxs_t, the shared expert's
 // term, if given], fp32, rounded once. Warp w of block (bx, by) owns token
@@ -294,6 +371,15 @@ cudaError_t launch_router_bwd_ep(const moe_config_t& c, const float* logits, con
       static_cast<__nv_bfloat16*>(dzb), Kp);
   return cudaGetLastError();
 }
+template <int EPL>
+cudaError_t launch_router_bwd_wide(const moe_config_t& c, const float* logits, const int32_t* idx,
+                                   const float* gate, const float* dg, const float* f,
+                                   float alpha, float* dz, void* dzb, int Kp, cudaStream_t s) {
+  bwd_router_wide_kernel<EPL><<<(c.T + NW - 1) / NW, NT, 0, s>>>(
+      logits, idx, gate, dg, f, alpha, c.tau, c.T, c.E, c.k, dz,
+      static_cast<__nv_bfloat16*>(dzb), Kp);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -333,9 +419,15 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
     case 32: return MOE_RB(32);
     case 48: return MOE_RB(48);
     case 64: return MOE_RB(64);
-    default: return cudaErrorInvalidValue;
+    default: break;
   }
 #undef MOE_RB
+  // Kp (a multiple of 64 >= E) <= 256: every padded column is in some lane's slots
+  if (c.E <= 128 && Kp <= 128)
+    return launch_router_bwd_wide<4>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+  if (c.E <= 256 && Kp <= 256)
+    return launch_router_bwd_wide<8>(c, logits, idx, gate, dg, f, alpha, dz, dzb, Kp, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,

@@ -86,8 +86,17 @@ struct SmemTail {
   uint32_t tmem_base;
   int abort_flag;
   int n_tiles_total;
-  int tbase[kMaxE + 1];
+  int n_heavy_tiles;        // tiles of the heavy experts (the first block of tbase)
+  int tbase[kMaxE + 1];     // first tile of each expert, in the order of perm
+  uint8_t perm[kMaxE];      // heavy experts by id, then light experts by id
 };
+
+// An expert with at most this many m-tiles is "light": each of its (expert,
+// n-tile) weight slabs serves one or two tiles, so its tiles read more bytes
+// from DRAM per MMA than DRAM can deliver to every SM at once. The others
+// ("heavy") reuse a slab over three or more tiles from L2 and are bound by the
+// tensor cores. See tile_info.
+constexpr int kLightMTiles = 2;
 
 // Epilogue staging: each epilogue warp writes its 32 rows x 32 columns of
 // bf16 output (2 KB) here and stores it with one TMA bulk tensor store, so
@@ -174,18 +183,31 @@ struct TileInfo {
 };
 
 // tile -> (expert, first row, end row of the expert, first output column);
-// the expert offsets are read through the read-only cache
+// the expert offsets are read through the read-only cache.
+// The tiles of light experts (weight streaming) are spread evenly among those
+// of heavy experts (tensor-bound) instead of all coming last: tile p is the
+// cl(p)-th light tile when cl(p) = floor((p+1) nL / total) steps up at p, else
+// the (p - cl(p))-th heavy tile, so every run of consecutive tiles (one wave
+// of the persistent grid) holds both kinds in the same proportion and the
+// weight streams overlap the MMAs. Within each kind the order stays expert by
+// expert, n-tile by n-tile, m-tile fastest (an n-tile's weight slab is read
+// by its m-tiles together, while it is in L2).
 template <int BM_T, class ST>
 __device__ __forceinline__ TileInfo tile_info(const ST& st, const int32_t* __restrict__ off,
                                               int E, int n_tiles_n, int tile, int bn_out) {
-  int lo = 0, hi = E - 1;  // largest e with tbase[e] <= tile
+  const int total = st.n_tiles_total, nH = st.n_heavy_tiles;
+  const int64_t nL = total - nH;
+  const int cl = (int)((int64_t)(tile + 1) * nL / total);
+  const int cp = (int)((int64_t)tile * nL / total);
+  const int q = cl > cp ? nH + cl - 1 : tile - cl;   // index in tbase order
+  int lo = 0, hi = E - 1;  // largest position with tbase[pos] <= q
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (st.tbase[mid] <= tile) lo = mid;
+    if (st.tbase[mid] <= q) lo = mid;
     else hi = mid - 1;
   }
-  const int e = lo;
-  const int local = tile - st.tbase[e];
+  const int e = st.perm[lo];
+  const int local = q - st.tbase[lo];
   const int o0 = __ldg(off + e), o1 = __ldg(off + e + 1);
   const int mt = (o1 - o0 + BM_T - 1) / BM_T;
   TileInfo ti;
@@ -274,34 +296,76 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
   }
   pdl_wait();
   const int n_tiles_n = (N + BN_OUT - 1) / BN_OUT;
-  if (warp == 2) {  // tbase[e] = sum_{e'<e} m-tiles(e') * n_tiles_n
+  if (warp == 2) {
+    // Tile table: experts in the order perm (heavy ones by id, then light
+    // ones by id), tbase[pos] = tiles of the experts before position pos,
+    // m-tiles(e) * n_tiles_n tiles each.
     // The offsets may be a caller's input (moe_expert_ffn): unless offset[0]
     // = 0 <= offset[1] <= ... <= offset[E] <= rows_limit, no tile runs (a
     // negative row would start a TMA store before the tensor) and the status
     // header records MOE_ERR_INVALID_ARG (where = 42).
-    int run = 0;
     bool bad = false;
-    for (int e0 = 0; e0 <= E; e0 += 32) {
-      const int e = e0 + lane;
+    int n_heavy_experts = 0, n_heavy_tiles = 0, n_tiles = 0;
+    int mts[kMaxE / 32];  // m-tiles of expert 32 i + lane
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {  // pass 1: check, count
+      if (32 * i >= E) break;
+      const int e = 32 * i + lane;
       int mt = 0;
       if (e < E) {
         const int lo = __ldg(offset + e), hi = __ldg(offset + e + 1);
         bad |= hi < lo || hi > rows_limit || (e == 0 && lo != 0);
         mt = bad ? 0 : (hi - lo + BM_T - 1) / BM_T;
       }
-      int incl = mt * n_tiles_n;
-      const int v = incl;
+      mts[i] = mt;
+      const bool heavy = mt > kLightMTiles;
+      n_heavy_experts += __popc(__ballot_sync(0xffffffffu, heavy));
+      int th = heavy ? mt * n_tiles_n : 0, t = mt * n_tiles_n;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+      for (int o = 16; o > 0; o >>= 1) {
+        th += __shfl_xor_sync(0xffffffffu, th, o);
+        t += __shfl_xor_sync(0xffffffffu, t, o);
       }
-      if (e <= E) st.tbase[e] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      n_heavy_tiles += th;
+      n_tiles += t;
     }
     bad = __any_sync(0xffffffffu, bad);
+    int rank_h = 0, rank_l = 0, base_h = 0, base_l = n_heavy_tiles;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {  // pass 2: positions, bases
+      if (bad || 32 * i >= E) break;
+      const int e = 32 * i + lane;
+      const int mt = mts[i];
+      const bool heavy = mt > kLightMTiles;
+      const unsigned hb = __ballot_sync(0xffffffffu, e < E && heavy);
+      const unsigned lb = __ballot_sync(0xffffffffu, e < E && !heavy);
+      const unsigned below = (1u << lane) - 1u;
+      int ih = heavy ? mt * n_tiles_n : 0, il = heavy ? 0 : mt * n_tiles_n;
+      const int vh = ih, vl = il;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nh = __shfl_up_sync(0xffffffffu, ih, o);
+        const int nl = __shfl_up_sync(0xffffffffu, il, o);
+        if (lane >= o) {
+          ih += nh;
+          il += nl;
+        }
+      }
+      if (e < E) {
+        const int pos = heavy ? rank_h + __popc(hb & below)
+                              : n_heavy_experts + rank_l + __popc(lb & below);
+        st.perm[pos] = (uint8_t)e;
+        st.tbase[pos] = heavy ? base_h + ih - vh : base_l + il - vl;
+      }
+      rank_h += __popc(hb);
+      rank_l += __popc(lb);
+      base_h += __shfl_sync(0xffffffffu, ih, 31);
+      base_l += __shfl_sync(0xffffffffu, il, 31);
+    }
     if (lane == 0) {
-      st.n_tiles_total = bad ? 0 : st.tbase[E];
+      st.tbase[E] = bad ? 0 : n_tiles;
+      st.n_heavy_tiles = bad ? 0 : n_heavy_tiles;
+      st.n_tiles_total = bad ? 0 : n_tiles;
       if (bad && hdr != nullptr && atomicCAS(hdr, 0, (int)MOE_ERR_INVALID_ARG) == 0)
         atomicExch(hdr + 1, 42);
     }

@@ -20,7 +20,12 @@
 // fp32 accumulators in TMEM), tiles (e, 128-row m tile, 256-column n tile)
 // with m fastest. A stage holds A as two boxes [64 rows x 64 m] and B as four
 // boxes [64 rows x 64 n]. The epilogue writes fp32 rows; an expert without
-// rows gets zeros.
+// rows gets zeros. Each epilogue warp turns its 32 rows x 32 columns around
+// in shared memory (4 KB) so that every store instruction writes four whole
+// 128-byte row segments: stored straight from the accumulator's layout (one
+// row per lane), each instruction would touch 32 rows with 16 bytes each,
+// and the long tail's weight gradients (2.2 GB of fp32, mostly experts with
+// a few rows, whose tiles are nothing but stores) went out at 1.8 TB/s.
 #include "moe_internal.h"
 #include "tc_ptx.cuh"
 
@@ -56,7 +61,9 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(Smem);
+constexpr int EPI_BYTES = 32 * 32 * 4;     // one warp's 32 x 32 fp32 block
+constexpr size_t SMEM_BYTES =
+    1024 + STAGES * (A_BYTES + B_BYTES) + EPI_WARPS * EPI_BYTES + sizeof(Smem);
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 // tile -> expert, first m and n, first row of the expert, its K blocks, the
@@ -94,7 +101,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  Smem& st = *reinterpret_cast<Smem*>(smem + STAGES * (A_BYTES + B_BYTES));
+  uint8_t* sE = smem + STAGES * (A_BYTES + B_BYTES);
+  Smem& st = *reinterpret_cast<Smem*>(sE + EPI_WARPS * EPI_BYTES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -297,7 +305,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 24)) break;
       tc_fence_after();
       const bool empty = w.nkb == 0;
-      const int m = w.m0 + quarter * 32 + lane;
       const int cbase = 128 * half;
       uint32_t r[128];
       if (!empty) {
@@ -317,18 +324,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
-      if (m < M) {
-        float* orow = m < m_split
-                          ? out + ((size_t)w.e * m_split + m) * N
-                          : out2 + ((size_t)w.e * (M - m_split) + (m - m_split)) * N;
+      // 32 columns at a time: lane = row writes its 16-byte pieces q at
+      // q ^ (row & 7) (eight rows' writes of one q cover all 32 banks); then
+      // lanes 8i .. 8i+7 read one row's 128 bytes and store them together
+      float* buf = reinterpret_cast<float*>(sE + ew * EPI_BYTES);
+      const int rr = lane >> 3, q = lane & 7;  // read side: row within 4, piece
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
-          const int n = w.n0 + cbase + j;
-          if (n + 4 <= N)
-            *reinterpret_cast<float4*>(orow + n) =
-                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+          *reinterpret_cast<uint4*>(buf + lane * 32 + ((p ^ (lane & 7)) << 2)) =
+              make_uint4(r[32 * ch + 4 * p], r[32 * ch + 4 * p + 1], r[32 * ch + 4 * p + 2],
+                         r[32 * ch + 4 * p + 3]);
+        __syncwarp();
+        const int n = w.n0 + cbase + 32 * ch + 4 * q;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + rr;
+          const int mm = w.m0 + quarter * 32 + row;
+          const float4 v =
+              *reinterpret_cast<const float4*>(buf + row * 32 + ((q ^ (row & 7)) << 2));
+          if (mm < M && n + 4 <= N) {
+            float* orow = mm < m_split
+                              ? out + ((size_t)w.e * m_split + mm) * N
+                              : out2 + ((size_t)w.e * (M - m_split) + (mm - m_split)) * N;
+            *reinterpret_cast<float4*>(orow + n) = v;
+          }
         }
+        __syncwarp();
       }
     }
   }

@@ -34,6 +34,11 @@ CASES = {
     "swiglu_ragged_h": (W.small(WL["mixtral"], T=640, d=136, H=200, E=5), 0.1, False),
     # std-scaled router noise: its strength carries no gradient
     "std_noise": (W.small(WL["sweep_std_noise"], T=1500, d=256, H=256), 0.1, False),
+    # more than 64 experts: the FMA router forward, the warp-per-token router
+    # backward (4 and 8 experts per lane), padded dz columns up to 128 and 256
+    "wide_e96_k4": (W.small(WL["longtail"], T=1200, d=128, H=128, E=96, k=4), 0.05, False),
+    "wide_e256_k8": (W.small(WL["sweep_e16_k4"], T=1024, d=64, H=128, E=256, k=8), 0.1, True),
+    "wide_e65_k1": (W.small(WL["switch_top1"], T=700, d=64, H=64, E=65, k=1), 0.2, False),
 }
 
 
