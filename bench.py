@@ -188,9 +188,11 @@ def bench_config(w, capacity: int, kept: int, n_active: int, nsets: int, fp: int
 def time_backward(w, cfg, inp, ws, stream, dev, kept, reps):
     """ms per moe_layer_backward call (loss = sum <dy, y> + 0.01 L_balance),
     and the tensor-core GEMM work it executes: the recomputed
-    pre-activations, dh = dY W2, dxd = dact [W1; W3] and the weight
-    gradients, kept * 2 * d * H * (3 (nm - 1) + 2) flops."""
+    pre-activations (unless cfg keeps them from the forward), dh = dY W2,
+    dxd = dact [W1; W3] and the weight gradients, kept * 2 * d * H *
+    (3 (nm - 1) + 2) flops, (nm - 1) fewer with kept pre-activations."""
     from mixture_experts_layer_99_b300 import moe
+    keep = bool(cfg.flags & moe.MOE_FLAG_KEEP_PREACT)
     out = moe.alloc_outputs(cfg, dev)
     moe.layer_forward(cfg, inp, ws=ws, out=out)
     dy = torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(5)).to(
@@ -207,11 +209,22 @@ def time_backward(w, cfg, inp, ws, stream, dev, kept, reps):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / reps
-    flops = kept * 2 * w.d * w.H * (3 * (w.nmat - 1) + 2)
+    # the forward of the same configuration, eager calls (with kept
+    # pre-activations its GEMM1 also stores them)
+    a.record(stream)
+    for _ in range(reps):
+        moe.layer_forward(cfg, inp, ws=ws, out=out)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_ms = a.elapsed_time(b) / reps
+    flops = kept * 2 * w.d * w.H * ((2 if keep else 3) * (w.nmat - 1) + 2)
     return dict(ms_per_call=ms, calls=reps, gemm_tflops_executed=flops / (ms / 1e3) / 1e12,
+                forward_ms_per_call=fwd_ms,
                 tokens_per_s=w.T / (ms / 1e3), loss="sum <dy, y> + 0.01 L_balance",
-                note="eager calls on one input set; GEMM work includes the recomputed "
-                     "pre-activations")
+                note=("eager calls on one input set; the forward kept the pre-activations "
+                      "(MOE_FLAG_KEEP_PREACT)" if keep else
+                      "eager calls on one input set; GEMM work includes the recomputed "
+                      "pre-activations"))
 
 
 def traffic_record(kernel_src_sha, workload):
@@ -574,8 +587,14 @@ def main():
     # ---- backward pass of the same layer call (moe_layer_backward), timed
     # alone with CUDA events after one forward call that left its state in ws
     bwd = None
-    if w.dtype == "bf16" and w.E <= 64 and w.shared_H == 0:
+    if w.dtype == "bf16" and w.shared_H == 0:
         bwd = time_backward(w, cfg, sets[0], ws, stream, dev, kept, max(3, args.steps // 20))
+        # a training forward that keeps the pre-activations, and its backward
+        cfg_k = moe.config_from_workload(w, keep_preact=True)
+        ws_k = moe.workspace(cfg_k, dev)
+        bwd["keep_preact"] = time_backward(w, cfg_k, sets[0], ws_k, stream, dev, kept,
+                                           max(3, args.steps // 20))
+        del ws_k
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -97,7 +97,18 @@ typedef struct {
   int32_t act;
   float tau;
   float noise_scale;
+  int32_t flags; /* MOE_FLAG_* bits; 0 for none */
 } moe_config_t;
+
+/* flags: moe_layer_forward[_shared] also keeps the experts' pre-activations
+ * (xd W1^T + b1 for GELU; gate xd W1^T and up xd W3^T for SwiGLU, bf16) in
+ * its workspace, and moe_layer_backward[_shared] reads them there instead of
+ * recomputing them (one GEMM1-sized product fewer per backward, and a
+ * smaller backward workspace). The forward workspace grows by
+ * min(T*k, E*C) * H * 2 bytes (GELU) or twice that (SwiGLU). Training only:
+ * the forward's outputs are the same either way. bf16 only
+ * (MOE_ERR_UNSUPPORTED for fp32). */
+#define MOE_FLAG_KEEP_PREACT 1
 
 /* Version of this ABI (major * 100 + minor). */
 MOE_API int32_t moe_abi_version(void);

@@ -48,6 +48,11 @@ WsLayout ws_layout(const moe_config_t& c, int /*num_sms*/, int H_shared) {
   L.P = take(E * 4);
   L.L = take(4);
   L.dropped = take(4);
+  // pre-activations kept by the forward for the backward: [R, H] (GELU) or
+  // [R, 2H] (SwiGLU, gate then up), bf16
+  L.pre = take((c.flags & MOE_FLAG_KEEP_PREACT)
+                   ? R * (size_t)c.H * (c.act == MOE_ACT_SWIGLU ? 2 : 1) * 2
+                   : 0);
   L.total_layer = off;
   L.x_stage = take(T * (size_t)c.d * s);
   L.y_stage = take(T * (size_t)c.d * s);
@@ -111,6 +116,8 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->d % align || c->H % align) return MOE_ERR_INVALID_ARG;
   if (!(c->tau > 0.f) || !isfinite(c->tau)) return MOE_ERR_INVALID_ARG;
   if (!(c->noise_scale >= 0.f) || !isfinite(c->noise_scale)) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~MOE_FLAG_KEEP_PREACT) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_KEEP_PREACT) && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->E > kMaxE || c->k > kMaxK) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->d >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED;
@@ -134,7 +141,7 @@ template <typename T> T* at(void* ws, size_t off) {
 
 extern "C" {
 
-int32_t moe_abi_version(void) { return 101; }
+int32_t moe_abi_version(void) { return 102; }
 
 const char* moe_status_string(int32_t status) {
   switch (status) {
@@ -315,7 +322,7 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
   }
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) {
-    if (fused_stats) {
+    if (c.dtype == MOE_BF16) {
       FfnFusion fz;
       fz.between = ev ? ev[3] : nullptr;
       if (scatter) {
@@ -323,6 +330,7 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
         fz.scatter_rows = token_of_row;
         fz.scatter_scale = gate;
       }
+      if (c.flags & MOE_FLAG_KEEP_PREACT) fz.keep_pre = at<void>(ws, L.pre);
       e = launch_ffn_tc(c, at<void>(ws, L.xd), offset, in->W1, in->W3, in->W2, in->b1, in->b2,
                         at<void>(ws, L.Y), at<void>(ws, L.ffn_h), R, at<int32_t>(ws, L.hdr), s,
                         &fz);
@@ -482,7 +490,8 @@ BwdLayout bwd_layout(const moe_config_t& c) {
     return at;
   };
   L.hdr = take(kHdrBytes);
-  L.pre = take(R * Hp * 2);
+  // recomputed pre-activations, unless the forward kept them in its workspace
+  L.pre = take((c.flags & MOE_FLAG_KEEP_PREACT) ? 0 : R * Hp * 2);
   L.dact = take(R * Hp * 2);
   L.dY = take(R * d * 2);
   L.dxd = take(R * d * 2);
@@ -589,7 +598,8 @@ static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer
   const void* xd = at<void>(wsm, L.xd);
   const void* Y = c.k > 1 ? at<void>(wsm, L.Y) : nullptr;  // k = 1: gates are identically 1
   const int32_t* off = fwd->expert_offset;
-  void* pre = at<void>(bws, B.pre);
+  const bool kept_pre = (c.flags & MOE_FLAG_KEEP_PREACT) != 0;
+  void* pre = kept_pre ? at<void>(wsm, L.pre) : at<void>(bws, B.pre);
   void* dact = at<void>(bws, B.dact);
   void* dYb = at<void>(bws, B.dY);
   void* dxd = at<void>(bws, B.dxd);
@@ -614,7 +624,7 @@ static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer
     e = launch_router_dx_tc(dzb, c.T, B.kp, in->Wg, c.E, c.d, goff, dxr, hdr, s);
   if (e == cudaSuccess)
     e = launch_ffn_bwd_tc(c, xd, off, in->W1, in->W3, in->b1, in->W2, W13T, dYb, pre, dact, dxd,
-                          R, hdr, s);
+                          R, hdr, s, kept_pre);
   // the shared expert: the same expert backward as one group of all T token
   // rows, its output gradient being dy itself (weight 1 for every token)
   void* dxs = nullptr;

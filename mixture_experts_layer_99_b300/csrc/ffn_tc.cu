@@ -218,6 +218,51 @@ __device__ __forceinline__ TileInfo tile_info(const ST& st, const int32_t* __res
   return ti;
 }
 
+// KEEP (the training forward's GEMM1): 32 pre-activation values of this
+// lane's row, columns col .. col + 31 of the kept [rows, ld] bf16 tensor, the
+// same way the epilogue stores its output: through the warp's staging buffer
+// and one TMA store when the warp's 32 rows all belong to the expert and the
+// columns fit (col_ok), else direct stores of a valid row's whole 8-column
+// pieces (up to ncols).
+template <int OUT_BUFS>
+__device__ __forceinline__ void keep_store(const float* vv, const CUtensorMap* map,
+                                           uint8_t* my_out0, int& n_stores, int lane,
+                                           bool full, bool row_ok, int col, int ncols,
+                                           int col_off, int wrow0, __nv_bfloat16* row_ptr) {
+  uint4 pk[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk[q]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      h2[j] = __floats2bfloat162_rn(vv[8 * q + 2 * j], vv[8 * q + 2 * j + 1]);
+  }
+  if (full) {
+    uint8_t* my_out = my_out0 + (n_stores % OUT_BUFS) * STAGE_OUT_BYTES;
+    ++n_stores;
+    if (lane == 0) {
+      if (OUT_BUFS == 1) bulk_wait_read0();
+      else bulk_wait_read<OUT_BUFS - 1>();
+    }
+    __syncwarp();
+    uint4* dst = reinterpret_cast<uint4*>(my_out + lane * 64);
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q ^ sw] = pk[q];
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, my_out, col + col_off, wrow0);
+      bulk_commit();
+    }
+  } else if (row_ok) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (col + 8 * q + 8 <= ncols)
+        *reinterpret_cast<uint4*>(row_ptr + col + col_off + 8 * q) = pk[q];
+  }
+}
+
 // PAIR: the kernel runs as clusters of two CTAs that share one 256-row tile
 // (see the cta_group::2 wrappers): each CTA loads its own 128 rows of A and
 // half of the B tile (gate rows for SwiGLU on rank 0, up rows on rank 1), so
@@ -230,19 +275,24 @@ __device__ __forceinline__ TileInfo tile_info(const ST& st, const int32_t* __res
 // backward's dY W2 and dact [W1; W3] products, no transposed copy of the
 // weights): per stage, boxes of [64 K rows x 64 N] side by side; with kb3 <
 // num_kb the K blocks from kb3 on come from tmB3 (W3 after W1).
-template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN>
+// KEEP (GELU and SwiGLU only): the epilogue also stores the pre-activations
+// (after the bias; gate and up for SwiGLU, the up half N columns further)
+// through tmKeep / keep, [rows, N] or [rows, 2N].
+template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN, bool KEEP = false>
 __global__ void __launch_bounds__(PIPE::THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmB3,
                            const __grid_constant__ CUtensorMap tmOut,
+                           const __grid_constant__ CUtensorMap tmKeep,
                            const int32_t* __restrict__ offset, int E, int N, int K,
                            const __nv_bfloat16* __restrict__ bias,
                            __nv_bfloat16* __restrict__ out, int32_t* __restrict__ hdr,
                            const int32_t* __restrict__ o_rows,
                            const float* __restrict__ o_scale,
                            const __nv_bfloat16* __restrict__ pre, int ldo, int kb3,
-                           int rows_limit) {
+                           int rows_limit, __nv_bfloat16* __restrict__ keep) {
+  static_assert(!KEEP || MODE == kGelu || MODE == kSwiglu, "KEEP is for GEMM1 only");
   constexpr int BN_OUT = MODE == kSwiglu ? 128 : UMMA_N;
   constexpr bool BWD = MODE == kBwdGelu || MODE == kBwdSwiglu;
   constexpr int STAGES = PIPE::STAGES;
@@ -614,6 +664,19 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
         float v[32];
         float v2[32];  // kBwdSwiglu: the second output (d up), stored N columns further
         if (MODE == kSwiglu) {
+          if constexpr (KEEP) {  // gate a at column n, up at column N + n
+            const bool kfull = warp_full && ti.n0 + c + 32 <= N;
+            __nv_bfloat16* krow = keep + (size_t)row * (2 * N);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              v[j] = __uint_as_float(r[32 * ch + j]);
+              v2[j] = __uint_as_float(r[OUTC + 32 * ch + j]);
+            }
+            keep_store<OUT_BUFS>(v, &tmKeep, my_out0, n_stores, lane, kfull, row_ok, ti.n0 + c,
+                                 N, 0, wrow0, krow);
+            keep_store<OUT_BUFS>(v2, &tmKeep, my_out0, n_stores, lane, kfull, row_ok, ti.n0 + c,
+                                 N, N, wrow0, krow);
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             v[j] = silu_f(__uint_as_float(r[32 * ch + j])) * __uint_as_float(r[OUTC + 32 * ch + j]);
@@ -661,6 +724,10 @@ __global__ void __launch_bounds__(PIPE::THREADS, 1)
               if (ti.n0 + c + j < N) v[j] += __bfloat162float(be[j]);
           }
           if (MODE == kGelu) {
+            if constexpr (KEEP)  // the pre-activation, bias added
+              keep_store<OUT_BUFS>(v, &tmKeep, my_out0, n_stores, lane,
+                                   warp_full && ti.n0 + c + 32 <= N, row_ok, ti.n0 + c, N, 0,
+                                   wrow0, keep + (size_t)row * N);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = gelu_as(v[j]);
           }
@@ -803,15 +870,16 @@ bool make_map_out(CUtensorMap* m, const void* base, uint64_t N, uint64_t rows,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN>
+template <int MODE, bool SCATTER, bool PAIR, class PIPE, bool BMN, bool KEEP = false>
 cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3,
                           const CUtensorMap& o, const int32_t* offset, int E, int N, int K,
                           const void* bias, void* out, int64_t rows_bound, int32_t* hdr,
                           const int32_t* o_rows, const float* o_scale, const void* pre,
-                          int ldo, int kb3, cudaStream_t s) {
+                          int ldo, int kb3, cudaStream_t s, const CUtensorMap* keep_map = nullptr,
+                          void* keep = nullptr) {
   constexpr size_t SMEM_BYTES = smem_bytes<PAIR, PIPE>();
-  auto kernel = grouped_gemm_tc_kernel<MODE, SCATTER, PAIR, PIPE, BMN>;
-  static int max_units[64] = {};  // per device: CTAs (or CTA pairs) resident at once
+  auto kernel = grouped_gemm_tc_kernel<MODE, SCATTER, PAIR, PIPE, BMN, KEEP>;
+  static int max_units[64] = {};  // per device and instantiation: CTAs (or pairs) at once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -845,10 +913,12 @@ cudaError_t launch_gemm_p(const CUtensorMap& a, const CUtensorMap& b, const CUte
   if (units < 1) units = 1;
   const unsigned grid = (unsigned)(PAIR ? 2 * units : units);
   return launch_pdl_cluster(kernel, dim3(grid), dim3(PIPE::THREADS), SMEM_BYTES, PAIR ? 2 : 1, s, a,
-                            b, b3, o, offset, E, N, K, static_cast<const __nv_bfloat16*>(bias),
+                            b, b3, o, keep_map ? *keep_map : o, offset, E, N, K,
+                            static_cast<const __nv_bfloat16*>(bias),
                             static_cast<__nv_bfloat16*>(out), hdr, o_rows, o_scale,
                             static_cast<const __nv_bfloat16*>(pre), ldo > 0 ? ldo : N, kb3,
-                            (int)(rows_bound < INT32_MAX ? rows_bound : INT32_MAX));
+                            (int)(rows_bound < INT32_MAX ? rows_bound : INT32_MAX),
+                            static_cast<__nv_bfloat16*>(keep));
 }
 
 // BMN (B MN-major): kb3 is the first K block read through b3 (< 0: none).
@@ -857,8 +927,20 @@ cudaError_t launch_gemm(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& b3, const CUtensorMap& o, const int32_t* offset, int E,
                         int N, int K, const void* bias, void* out, int64_t rows_bound,
                         int32_t* hdr, const int32_t* o_rows, const float* o_scale,
-                        cudaStream_t s, const void* pre = nullptr, int ldo = 0, int kb3 = -1) {
+                        cudaStream_t s, const void* pre = nullptr, int ldo = 0, int kb3 = -1,
+                        const CUtensorMap* keep_map = nullptr, void* keep = nullptr) {
   if (!BMN || kb3 < 0) kb3 = (K + BK - 1) / BK;
+  if constexpr ((MODE == kGelu || MODE == kSwiglu) && !SCATTER && !BMN) {
+    if (keep) {
+      if (pair)
+        return launch_gemm_p<MODE, false, true, PipePairShape, false, true>(
+            a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo,
+            kb3, s, keep_map, keep);
+      return launch_gemm_p<MODE, false, false, PipeShape, false, true>(
+          a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo,
+          kb3, s, keep_map, keep);
+    }
+  }
   if (pair)
     return launch_gemm_p<MODE, SCATTER, true, PipePairShape, BMN>(
         a, b, b3, o, offset, E, N, K, bias, out, rows_bound, hdr, o_rows, o_scale, pre, ldo, kb3,
@@ -933,13 +1015,21 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
     return cudaErrorInvalidValue;
   if (swiglu && !make_map_3d(&mw3, W3, c.d, c.H, c.E, 128)) return cudaErrorInvalidValue;
   if (!swiglu) mw3 = mw1;
+  // the pre-activations kept for the backward: [R, H] (GELU, bias added) or
+  // [R, 2H] (SwiGLU: gate, then up)
+  CUtensorMap mkeep;
+  void* keep = fz ? fz->keep_pre : nullptr;
+  if (keep && !make_map_out(&mkeep, keep, swiglu ? 2 * (uint64_t)c.H : (uint64_t)c.H, R))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   if (swiglu)
     e = launch_gemm<kSwiglu, false>(pair, mx, mw1, mw3, moh, offset, c.E, c.H, c.d, nullptr, h,
-                                    rows_bound, hdr, nullptr, nullptr, s);
+                                    rows_bound, hdr, nullptr, nullptr, s, nullptr, 0, -1,
+                                    keep ? &mkeep : nullptr, keep);
   else
     e = launch_gemm<kGelu, false>(pair, mx, mw1, mw3, moh, offset, c.E, c.H, c.d, b1, h,
-                                  rows_bound, hdr, nullptr, nullptr, s);
+                                  rows_bound, hdr, nullptr, nullptr, s, nullptr, 0, -1,
+                                  keep ? &mkeep : nullptr, keep);
   if (e != cudaSuccess) return e;
   if (fz && fz->between && (e = record_stage_event(fz->between, s)) != cudaSuccess) return e;
   const void* b2e = swiglu ? nullptr : b2;
@@ -957,11 +1047,13 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
 // The weights are read as stored (W2 [E, d, H], W1 and W3 [E, H, d]: B
 // MN-major); W13T [E, d, Hp] (Hp = 2H), the transposed [W1; W3], is used only
 // by a SwiGLU hidden size that is not a multiple of 64 (else NULL). The
-// pre-activations are recomputed here rather than kept from the forward pass.
+// pre-activations are recomputed into pre, unless have_pre (the forward kept
+// them there).
 cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                               const void* W1, const void* W3, const void* b1, const void* W2,
                               const void* W13T, const void* dY, void* pre, void* dact,
-                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s) {
+                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s,
+                              bool have_pre) {
   const uint64_t R = (uint64_t)rows_bound;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   const bool pair = use_pairs(c);
@@ -973,13 +1065,14 @@ cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32
       !make_map_3d(&mw2n, W2, H, d, c.E, BK) || !make_map_out(&mdact_o, dact, Hp, R) ||
       !make_map_2d(&mdact_a, dact, Hp, R) || !make_map_out(&mdxd, dxd, d, R))
     return cudaErrorInvalidValue;
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
   // recomputed pre-activations
-  e = launch_gemm<kPlain, false>(pair, mxd, mw1, mw1, mpa, offset, c.E, c.H, c.d,
-                                 swiglu ? nullptr : b1, pre, rows_bound, hdr, nullptr, nullptr, s,
-                                 nullptr, (int)Hp);
+  if (!have_pre)
+    e = launch_gemm<kPlain, false>(pair, mxd, mw1, mw1, mpa, offset, c.E, c.H, c.d,
+                                   swiglu ? nullptr : b1, pre, rows_bound, hdr, nullptr, nullptr,
+                                   s, nullptr, (int)Hp);
   if (e != cudaSuccess) return e;
-  if (swiglu) {
+  if (swiglu && !have_pre) {
     if (!make_map_3d(&mw3, W3, d, H, c.E, box) ||
         !make_map_out(&mpv, static_cast<__nv_bfloat16*>(pre) + H, H, R, Hp))
       return cudaErrorInvalidValue;

@@ -155,7 +155,7 @@ struct WsLayout {
   size_t hdr, router_partial, router_tile_hist, router_split, disp_hist, disp_base, ffn_h, ffn_sched;
   // fused layer intermediates
   size_t logits, topk_idx, topk_gate, slot_of, count, offset, token_of_row, xd, Y,
-      prob_sum, f, P, L, dropped;
+      prob_sum, f, P, L, dropped, pre;
   // host-io staging
   size_t x_stage, y_stage;
   size_t total_core, total_layer, total_host;
@@ -205,6 +205,7 @@ struct FfnFusion {
   const int32_t* scatter_rows = nullptr;  // token_of_row, or nullptr (k = 1 only)
   const float* scatter_scale = nullptr;   // topk_gate [T] (k = 1)
   cudaEvent_t between = nullptr;          // recorded between GEMM1 and GEMM2, if set
+  void* keep_pre = nullptr;               // GEMM1 also stores its pre-activations here
 };
 cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                           const void* W1, const void* W3, const void* W2, const void* b1,
@@ -225,7 +226,8 @@ inline bool bwd_w13_transposed(const moe_config_t& c) {
 cudaError_t launch_ffn_bwd_tc(const moe_config_t& c, const void* xd, const int32_t* offset,
                               const void* W1, const void* W3, const void* b1, const void* W2,
                               const void* W13T, const void* dY, void* pre, void* dact,
-                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s);
+                              void* dxd, int64_t rows_bound, int32_t* hdr, cudaStream_t s,
+                              bool have_pre = false);
 cudaError_t launch_router_dx_tc(const void* dz_bf16, int T, int Kp, const void* Wg, int E, int d,
                                 const int32_t* off, void* dxr, int32_t* hdr, cudaStream_t s);
 cudaError_t launch_wgrad_tc(const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -45,12 +45,16 @@ class MoEError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("T", c_int32), ("d", c_int32), ("E", c_int32), ("k", c_int32),
                 ("H", c_int32), ("capacity", c_int32), ("dtype", c_int32),
-                ("act", c_int32), ("tau", c_float), ("noise_scale", c_float)]
+                ("act", c_int32), ("tau", c_float), ("noise_scale", c_float),
+                ("flags", c_int32)]
 
     def __repr__(self):
         return (f"Config(T={self.T}, d={self.d}, E={self.E}, k={self.k}, H={self.H}, "
                 f"C={self.capacity}, dtype={self.dtype}, act={self.act}, tau={self.tau}, "
-                f"noise_scale={self.noise_scale})")
+                f"noise_scale={self.noise_scale}, flags={self.flags})")
+
+
+MOE_FLAG_KEEP_PREACT = 1
 
 
 class LayerInputs(ctypes.Structure):
@@ -149,16 +153,18 @@ def capacity(c, k: int, T: int, E: int) -> int:
 
 
 def make_config(T, d, E, k, H, capacity_, dtype="bf16", act="gelu", tau=1.0,
-                noise_scale=0.0) -> Config:
+                noise_scale=0.0, keep_preact=False) -> Config:
+    """keep_preact: the forward keeps the experts' pre-activations in its
+    workspace for the backward (MOE_FLAG_KEEP_PREACT)."""
     return Config(T, d, E, k, H, capacity_, MOE_F32 if dtype == "f32" else MOE_BF16,
                   MOE_ACT_GELU if act == "gelu" else MOE_ACT_SWIGLU, float(tau),
-                  float(noise_scale))
+                  float(noise_scale), MOE_FLAG_KEEP_PREACT if keep_preact else 0)
 
 
-def config_from_workload(w, T: Optional[int] = None) -> Config:
+def config_from_workload(w, T: Optional[int] = None, keep_preact: bool = False) -> Config:
     T = w.T if T is None else T
     return make_config(T, w.d, w.E, w.k, w.H, capacity(w.c, w.k, T, w.E), w.dtype, w.act,
-                       w.tau, w.noise_scale)
+                       w.tau, w.noise_scale, keep_preact)
 
 
 def _dt(cfg):

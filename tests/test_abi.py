@@ -34,9 +34,10 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     L = moe.lib()
-    # 1.01: moe_config_t carries noise_scale (std-scaled router noise)
-    assert L.moe_abi_version() == 101
-    assert ctypes.sizeof(moe.Config) == 10 * 4
+    # 1.01: moe_config_t carries noise_scale (std-scaled router noise);
+    # 1.02: and flags (MOE_FLAG_KEEP_PREACT)
+    assert L.moe_abi_version() == 102
+    assert ctypes.sizeof(moe.Config) == 11 * 4
     for code in range(6):
         assert L.moe_status_string(code)
     assert L.moe_status_string(99) == b"unknown status"
@@ -72,11 +73,37 @@ def test_invalid_config_rejected(bad):
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("bad", [dict(E=300, k=2), dict(E=16, k=9)])
+@pytest.mark.parametrize("bad", [dict(E=300, k=2), dict(E=16, k=9),
+                                 dict(dtype="f32", keep_preact=True)])
 def test_unsupported_config(bad):
     with pytest.raises(moe.MoEError) as ei:
         moe.workspace_size(_cfg(**bad))
     assert ei.value.status == 2
+
+
+def test_unknown_flags_rejected():
+    for bad in (2, 4, 1 << 30, -1):
+        cfg = _cfg()
+        cfg.flags = bad
+        with pytest.raises(moe.MoEError) as ei:
+            moe.workspace_size(cfg)
+        assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("act,mult", [("gelu", 1), ("swiglu", 2)])
+def test_keep_preact_workspace(act, mult):
+    """The forward workspace grows by the kept pre-activations (bf16 rows of
+    H, or 2H for SwiGLU); the backward workspace loses its copy of them."""
+    a, b = _cfg(act=act), _cfg(act=act, keep_preact=True)
+    R = min(a.T * a.k, a.E * a.capacity)
+    grow = moe.workspace_size(b) - moe.workspace_size(a)
+    # (regions are 256-byte aligned, and an empty one still takes 256 bytes)
+    assert R * a.H * mult * 2 - 256 <= grow <= R * a.H * mult * 2 + 256
+    L = moe.lib()
+    na, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.moe_workspace_size_backward(ctypes.byref(a), ctypes.byref(na)) == 0
+    assert L.moe_workspace_size_backward(ctypes.byref(b), ctypes.byref(nb)) == 0
+    assert na.value - nb.value >= R * a.H * mult * 2 - 256
 
 
 def test_workspace_size_grows_with_shape():

@@ -42,7 +42,7 @@ CASES = {
 }
 
 
-def _run(w, alpha, with_bias, seed=0):
+def _run(w, alpha, with_bias, seed=0, keep_preact=False):
     inp = W.make_inputs(w, seed)
     if with_bias:  # nonzero expert biases for the GELU bias gradients
         g = torch.Generator().manual_seed(seed + 99)
@@ -50,13 +50,33 @@ def _run(w, alpha, with_bias, seed=0):
         inp["b2"] = (0.1 * torch.randn(w.E, w.d, generator=g)).to(w.torch_dtype)
     gdy = torch.Generator().manual_seed(seed + 7)
     dy = torch.randn(w.T, w.d, generator=gdy).to(w.torch_dtype)
-    cfg = moe.config_from_workload(w)
+    cfg = moe.config_from_workload(w, keep_preact=keep_preact)
     dinp = W.to_device(inp, DEV)
     ws = moe.workspace(cfg, DEV)
     out = moe.layer_forward(cfg, dinp, ws=ws)
     grads = moe.layer_backward(cfg, dinp, out, dy.to(DEV), alpha, ws=ws)
     torch.cuda.synchronize()
     return inp, dy, cfg, out, grads
+
+
+@pytest.mark.parametrize("name", ["switch_small", "switch_pairs", "mixtral_pairs",
+                                  "longtail_small", "swiglu_ragged_h", "ragged_dims",
+                                  "wide_e96_k4"])
+def test_kept_preactivations_give_identical_results(name):
+    """MOE_FLAG_KEEP_PREACT: GEMM1's epilogue stores the pre-activations it
+    computes and the backward reads them instead of recomputing them with the
+    same kernel, so the forward outputs and every gradient are bit-identical
+    to the recomputing path."""
+    w, alpha, with_bias = CASES[name]
+    _, _, _, out0, g0 = _run(w, alpha, with_bias)
+    _, _, cfg, out1, g1 = _run(w, alpha, with_bias, keep_preact=True)
+    assert cfg.flags == moe.MOE_FLAG_KEEP_PREACT
+    for key, v in out0.items():
+        if isinstance(v, torch.Tensor):
+            assert torch.equal(v, out1[key]), key
+    for key, v in g0.items():
+        if v is not None:
+            assert torch.equal(v, g1[key]), key
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
