@@ -14,6 +14,8 @@
 // Every sum runs in a fixed order, so results are run-to-run identical.
 #include "moe_internal.h"
 
+#include <type_traits>
+
 namespace moe {
 namespace {
 
@@ -230,53 +232,61 @@ __global__ void __launch_bounds__(NT) bwd_router_wide_kernel(
 // dx_t = sum over the kept slots of dxd[slot] (slot order) + dxr_t (the
 // router term dz_t W_g from the tensor cores) [+ dxs_t, the shared expert's
 // term, if given], fp32, rounded once. Warp w of block (bx, by) owns token
-// bx * NW + w and a chunk of 128 16-byte vectors.
-constexpr int DX_UNR = 4, DX_CHUNK = 32 * DX_UNR;
+// bx * NW + w and a chunk of 32 UNR 16-byte vectors. Every lane issues all of
+// its loads (each slot's, dxr's and dxs's) before it adds them in that order.
+template <int KM>
+struct DxShape {
+  static constexpr int UNR = KM <= 2 ? 4 : (KM <= 4 ? 2 : 1);
+  static constexpr int CHUNK = 32 * UNR;
+};
+template <int KM>
 __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dxd,
                                                     const int32_t* __restrict__ slot_of,
                                                     const uint4* __restrict__ dxr, int T, int k,
                                                     int nvec, uint4* __restrict__ dx,
                                                     const uint4* __restrict__ dxs) {
+  constexpr int UNR = DxShape<KM>::UNR;
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T) return;
   const int lane = threadIdx.x & 31;
-  const int v0 = blockIdx.y * DX_CHUNK + lane;
-  float acc[DX_UNR][8];
+  const int v0 = blockIdx.y * DxShape<KM>::CHUNK + lane;
+  int sl[KM];
 #pragma unroll
-  for (int u = 0; u < DX_UNR; ++u)
+  for (int j = 0; j < KM; ++j) sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
+  uint4 q[KM][UNR], qr[UNR], qs[UNR];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int sl = slot_of[(size_t)t * k + j];
-    if (sl < 0) continue;
-    uint4 q[DX_UNR];
+  for (int u = 0; u < UNR; ++u) {
+    const int v = v0 + 32 * u;
+    const bool in = v < nvec;
 #pragma unroll
-    for (int u = 0; u < DX_UNR; ++u) {
-      const int v = v0 + 32 * u;
-      q[u] = v < nvec ? __ldg(dxd + (size_t)sl * nvec + v) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < DX_UNR; ++u) {
-      float a[8];
-      unpack8(q[u], a);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
-    }
+    for (int j = 0; j < KM; ++j)
+      q[j][u] = in && sl[j] >= 0 ? __ldg(dxd + (size_t)sl[j] * nvec + v) : make_uint4(0, 0, 0, 0);
+    qr[u] = in ? __ldg(dxr + (size_t)t * nvec + v) : make_uint4(0, 0, 0, 0);
+    qs[u] = in && dxs ? __ldg(dxs + (size_t)t * nvec + v) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int u = 0; u < DX_UNR; ++u) {
+  for (int u = 0; u < UNR; ++u) {
     const int v = v0 + 32 * u;
     if (v >= nvec) continue;
-    float a[8];
-    unpack8(__ldg(dxr + (size_t)t * nvec + v), a);
+    float acc[8], a[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
-    if (dxs) {
-      unpack8(__ldg(dxs + (size_t)t * nvec + v), a);
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[u][i] += a[i];
+    for (int j = 0; j < KM; ++j) {
+      if (sl[j] < 0) continue;
+      unpack8(q[j][u], a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += a[i];
     }
-    dx[(size_t)t * nvec + v] = pack8(acc[u]);
+    unpack8(qr[u], a);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += a[i];
+    if (dxs) {
+      unpack8(qs[u], a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += a[i];
+    }
+    dx[(size_t)t * nvec + v] = pack8(acc);
   }
 }
 
@@ -433,11 +443,18 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
                           const void* dxr, void* dx, cudaStream_t s, const void* dxs) {
   const int nvec = c.d / 8;
-  const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + DX_CHUNK - 1) / DX_CHUNK));
-  bwd_dx_kernel<<<grid, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of,
-                                    static_cast<const uint4*>(dxr), c.T, c.k, nvec,
-                                    static_cast<uint4*>(dx), static_cast<const uint4*>(dxs));
-  return cudaGetLastError();
+  auto go = [&](auto km) {
+    constexpr int KM = decltype(km)::value;
+    constexpr int CH = DxShape<KM>::CHUNK;
+    const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CH - 1) / CH));
+    bwd_dx_kernel<KM><<<grid, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of,
+                                          static_cast<const uint4*>(dxr), c.T, c.k, nvec,
+                                          static_cast<uint4*>(dx), static_cast<const uint4*>(dxs));
+    return cudaGetLastError();
+  };
+  if (c.k <= 2) return go(std::integral_constant<int, 2>{});
+  if (c.k <= 4) return go(std::integral_constant<int, 4>{});
+  return go(std::integral_constant<int, kMaxK>{});
 }
 
 // dWg = dz^T x on the tensor cores: token groups of the weight-gradient GEMM
