@@ -46,6 +46,13 @@
  *     (MOE_ERR_DEVICE_TIMEOUT), or a device-resident input of moe_dispatch or
  *     moe_expert_ffn out of range (MOE_ERR_INVALID_ARG; the host cannot check
  *     those without a synchronisation).
+ *   - Checked build (libmoe_b300_check.so, compiled with MOE_CHECK): every
+ *     kernel that indexes with rows, slots or tokens another kernel wrote
+ *     (the dispatch's row positions, the gather's tokens, the combine's and
+ *     the backward's slots) tests each index against its bound, skips the
+ *     access if it fails and records MOE_ERR_DEVICE_CHECK (where = 51..56).
+ *     The same calls, the same results; a debugging aid where no memory
+ *     checker can run.
  *   - Limits: 1 <= k <= 8, k <= E <= 256, T >= 1, T*k < 2^31, capacity >= 1;
  *     d and H multiples of 8 (bf16) or 4 (fp32); activations must be finite.
  */
@@ -73,7 +80,8 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,    /* valid but outside this build (e.g. k > 8)      */
   MOE_ERR_WORKSPACE = 3,      /* ws too small or misaligned                     */
   MOE_ERR_CUDA = 4,           /* a CUDA runtime call or kernel launch failed    */
-  MOE_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait ran out             */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out             */
+  MOE_ERR_DEVICE_CHECK = 6    /* checked build: an index out of its bounds       */
 } moe_status_t;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
@@ -131,11 +139,14 @@ MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t 
 
 /* Read and clear the device status word in ws. Synchronises `stream`.
  * *code is MOE_OK, or the first status a kernel recorded since the last read
- * (MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_INVALID_ARG). *where says which kernel
+ * (MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_INVALID_ARG or MOE_ERR_DEVICE_CHECK).
+ * *where says which kernel
  * recorded it (0 if none): 1..6 a wait of the grouped GEMM (roles: producer,
  * MMA issuer, epilogue), 41 an expert id outside [0, E) in moe_dispatch, 42 /
  * 43 bad expert offsets in moe_expert_ffn (bf16 / fp32 kernel), 11..14 a
- * wait of the tensor-core router, 21..27 a wait of the weight-gradient GEMM. */
+ * wait of the tensor-core router, 21..27 a wait of the weight-gradient GEMM;
+ * checked builds: 51 a gathered token, 52 a combined slot, 53 a dispatched
+ * row, 55 / 56 a slot in the backward's combine / dx sum. */
 MOE_API moe_status_t moe_device_status(void *ws, int32_t *code, int32_t *where,
                                moe_stream_t stream);
 

@@ -1,9 +1,11 @@
 """Build the in-tree CUDA library ``libmoe_b300.so`` for sm_103a with nvcc.
 
-Usage: ``python -m mixture_experts_layer_99_b300.build`` (or ``build()``).
-The library is placed next to this file so that it travels with the source
-tree; it links the CUDA runtime statically and needs no other CUDA library at
-load time.
+Usage: ``python -m mixture_experts_layer_99_b300.build [--check]`` (or
+``build()``). The library is placed next to this file so that it travels with
+the source tree; it links the CUDA runtime statically and needs no other CUDA
+library at load time. ``--check`` (``build(check=True)``) builds the checked
+variant ``libmoe_b300_check.so`` (-DMOE_CHECK: index checks in the kernels
+that index with data another kernel wrote; the same ABI).
 """
 from __future__ import annotations
 
@@ -15,6 +17,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
+LIB_CHECK = os.path.join(HERE, "libmoe_b300_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_tiles.cu", "dispatch_static.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu", "backward.cu", "ffn_wgrad_tc.cu"]
 
@@ -29,16 +32,18 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
+def build(verbose: bool = False, extra: list[str] | None = None, check: bool = False) -> str:
     """Compile every source to an object file (in parallel, one nvcc per
-    file, objects under _build/ beside the sources) and link the shared
-    library."""
+    file, objects under _build/ or _build_check/ beside the sources) and link
+    the shared library."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES if os.path.exists(os.path.join(CSRC, s))]
-    objdir = os.path.join(HERE, "_build")
+    lib = LIB_CHECK if check else LIB
+    extra = [*(extra or []), *(["-DMOE_CHECK"] if check else [])]
+    objdir = os.path.join(HERE, "_build_check" if check else "_build")
     os.makedirs(objdir, exist_ok=True)
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo", *ARCH,
               "-Xcompiler", "-fvisibility=hidden", "-DMOE_BUILD_SO",
-              "-I", os.path.join(HERE, "..", "include"), *(extra or [])]
+              "-I", os.path.join(HERE, "..", "include"), *extra]
     objs, procs = [], []
     for src in srcs:
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
@@ -57,16 +62,16 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
         elif verbose and out:
             print(out)
     if failed:
-        raise RuntimeError("nvcc failed building libmoe_b300.so")
-    cmd = [nvcc_path(), "-shared", *ARCH, "-cudart", "static", "-o", LIB + ".tmp", *objs]
+        raise RuntimeError(f"nvcc failed building {os.path.basename(lib)}")
+    cmd = [nvcc_path(), "-shared", *ARCH, "-cudart", "static", "-o", lib + ".tmp", *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed linking libmoe_b300.so")
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+        raise RuntimeError(f"nvcc failed linking {os.path.basename(lib)}")
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose="-v" in sys.argv, extra=[a for a in sys.argv[1:] if a != "-v"])
-    print(LIB)
+    args = [a for a in sys.argv[1:] if a not in ("-v", "--check")]
+    print(build(verbose="-v" in sys.argv, extra=args, check="--check" in sys.argv))

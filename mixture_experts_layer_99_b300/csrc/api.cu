@@ -151,6 +151,7 @@ const char* moe_status_string(int32_t status) {
     case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side index check failed";
     default: return "unknown status";
   }
 }
@@ -313,11 +314,15 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
     if (fused_stats) {
       e = launch_dispatch_from_router(c, idx, at<int32_t>(ws, L.router_tile_hist), partial,
                                       rgrid, count, offset, slot_of, token_of_row, prob_sum, f,
-                                      P, Lb, dropped, scatter ? y : nullptr, s);
-      if (e == cudaSuccess) e = launch_gather(c, x, token_of_row, offset, at<void>(ws, L.xd), R, s);
+                                      P, Lb, dropped, scatter ? y : nullptr, s,
+                                      at<int32_t>(ws, L.hdr));
+      if (e == cudaSuccess)
+        e = launch_gather(c, x, token_of_row, offset, at<void>(ws, L.xd), R, s,
+                          at<int32_t>(ws, L.hdr));
     } else {
       e = launch_dispatch(c, idx, x, count, offset, slot_of, token_of_row, at<void>(ws, L.xd),
-                          at<int32_t>(ws, L.disp_hist), at<int32_t>(ws, L.disp_base), R, s);
+                          at<int32_t>(ws, L.disp_hist), at<int32_t>(ws, L.disp_base), R, s,
+                          at<int32_t>(ws, L.hdr));
     }
   }
   if (e == cudaSuccess) e = mark(2);
@@ -357,7 +362,7 @@ static moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* x,
     base = at<void>(ws, L.sh_y);
   }
   if (e == cudaSuccess && !scatter)
-    e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s, base);
+    e = launch_combine(c, at<void>(ws, L.Y), slot_of, gate, y, s, base, at<int32_t>(ws, L.hdr));
   if (!fused_stats) {
     if (e == cudaSuccess) e = launch_prob_reduce(c, partial, rgrid, prob_sum, s);
     if (e == cudaSuccess) e = launch_aux(c, count, prob_sum, nullptr, 0, f, P, Lb, dropped, s);
@@ -611,7 +616,8 @@ static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer
     e = launch_weight_transpose(in->W1, c.E, c.H, c.d, Hp, 0, W13T, s);
     if (e == cudaSuccess) e = launch_weight_transpose(in->W3, c.E, c.H, c.d, Hp, c.H, W13T, s);
   }
-  if (e == cudaSuccess) e = launch_bwd_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s);
+  if (e == cudaSuccess)
+    e = launch_bwd_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s, hdr);
   void* dzb = at<void>(bws, B.dzb);
   void* dxr = at<void>(bws, B.dxr);
   int32_t* goff = at<int32_t>(bws, B.goff);
@@ -654,7 +660,7 @@ static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer
     if (e == cudaSuccess && sg->db1) e = launch_expert_colsum(dact_s, Hps, Hs, soff, 1, sg->db1, s);
     if (e == cudaSuccess && sg->db2) e = launch_expert_colsum(dy, c.d, c.d, soff, 1, sg->db2, s);
   }
-  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s, dxs);
+  if (e == cudaSuccess) e = launch_bwd_dx(c, dxd, fwd->slot_of, dxr, g->dx, s, dxs, hdr);
   if (e == cudaSuccess)
     e = launch_bwd_wg(c, dz, dzb, B.kp, in->x, at<int32_t>(bws, B.wgoff),
                       at<float>(bws, B.wg_part), g->dWg, g->dbias, hdr, s);

@@ -47,12 +47,14 @@ __global__ void __launch_bounds__(NT) bwd_combine_kernel(const uint4* __restrict
                                                          const float* __restrict__ gate, int T,
                                                          int k, int nvec,
                                                          uint4* __restrict__ dY,
-                                                         float* __restrict__ dg) {
+                                                         float* __restrict__ dg, int64_t rows_cap,
+                                                         int32_t* __restrict__ chk) {
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T) return;
   const int lane = threadIdx.x & 31;
   for (int j = 0; j < k; ++j) {
-    const int sl = slot_of[(size_t)t * k + j];
+    int sl = slot_of[(size_t)t * k + j];
+    if (!moe_check(sl < rows_cap, chk, 55)) sl = -1;
     const float g = gate[(size_t)t * k + j];
     float dot = 0.f;
     if (sl >= 0) {
@@ -244,7 +246,8 @@ __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dx
                                                     const int32_t* __restrict__ slot_of,
                                                     const uint4* __restrict__ dxr, int T, int k,
                                                     int nvec, uint4* __restrict__ dx,
-                                                    const uint4* __restrict__ dxs) {
+                                                    const uint4* __restrict__ dxs,
+                                                    int64_t rows_cap, int32_t* __restrict__ chk) {
   constexpr int UNR = DxShape<KM>::UNR;
   const int t = blockIdx.x * NW + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -252,7 +255,10 @@ __global__ void __launch_bounds__(NT) bwd_dx_kernel(const uint4* __restrict__ dx
   const int v0 = blockIdx.y * DxShape<KM>::CHUNK + lane;
   int sl[KM];
 #pragma unroll
-  for (int j = 0; j < KM; ++j) sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
+  for (int j = 0; j < KM; ++j) {
+    sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
+    if (!moe_check(sl[j] < rows_cap, chk, 56)) sl[j] = -1;
+  }
   uint4 q[KM][UNR], qr[UNR], qs[UNR];
 #pragma unroll
   for (int u = 0; u < UNR; ++u) {
@@ -410,11 +416,11 @@ int bwd_wg_group_tokens(const moe_config_t& c) {
 
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
                                const int32_t* slot_of, const float* gate, void* dY, float* dg,
-                               cudaStream_t s) {
+                               cudaStream_t s, int32_t* chk) {
   const int nvec = c.d / 8;
   bwd_combine_kernel<<<(c.T + NW - 1) / NW, NT, 0, s>>>(
       static_cast<const uint4*>(dy), static_cast<const uint4*>(Y), slot_of, gate, c.T, c.k, nvec,
-      static_cast<uint4*>(dY), dg);
+      static_cast<uint4*>(dY), dg, (int64_t)max_rows(c), chk);
   return cudaGetLastError();
 }
 
@@ -441,7 +447,8 @@ cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const 
 }
 
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const void* dxr, void* dx, cudaStream_t s, const void* dxs) {
+                          const void* dxr, void* dx, cudaStream_t s, const void* dxs,
+                          int32_t* chk) {
   const int nvec = c.d / 8;
   auto go = [&](auto km) {
     constexpr int KM = decltype(km)::value;
@@ -449,7 +456,8 @@ cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t*
     const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CH - 1) / CH));
     bwd_dx_kernel<KM><<<grid, NT, 0, s>>>(static_cast<const uint4*>(dxd), slot_of,
                                           static_cast<const uint4*>(dxr), c.T, c.k, nvec,
-                                          static_cast<uint4*>(dx), static_cast<const uint4*>(dxs));
+                                          static_cast<uint4*>(dx), static_cast<const uint4*>(dxs),
+                                          (int64_t)max_rows(c), chk);
     return cudaGetLastError();
   };
   if (c.k <= 2) return go(std::integral_constant<int, 2>{});

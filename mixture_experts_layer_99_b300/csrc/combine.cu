@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y
                                                      const int32_t* __restrict__ slot_of,
                                                      const float* __restrict__ gate, int T_,
                                                      int k, int nvec, uint4* __restrict__ y,
-                                                     const uint4* __restrict__ base) {
+                                                     const uint4* __restrict__ base,
+                                                     int64_t rows_cap, int32_t* __restrict__ chk) {
   constexpr int V = 16 / sizeof(T);
   constexpr int UNR = CombineShape<KM>::UNR;
   pdl_wait();
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint4* __restrict__ Y
 #pragma unroll
   for (int j = 0; j < KM; ++j) {
     sl[j] = j < k ? slot_of[(size_t)t * k + j] : -1;
+    if (!moe_check(sl[j] < rows_cap, chk, 52)) sl[j] = -1;
     g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
     if (first < 0 && sl[j] >= 0) first = sl[j];
   }
@@ -174,25 +176,27 @@ __global__ void __launch_bounds__(NT) aux_kernel(const int32_t* __restrict__ cou
 
 template <int KM>
 cudaError_t launch_combine_km(const moe_config_t& c, const uint4* Y, const int32_t* slot_of,
-                              const float* gate, uint4* y, const uint4* b, cudaStream_t s) {
+                              const float* gate, uint4* y, const uint4* b, cudaStream_t s,
+                              int32_t* chk) {
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   constexpr int CHUNK = CombineShape<KM>::CHUNK;
   const dim3 grid((unsigned)((c.T + NW - 1) / NW), (unsigned)((nvec + CHUNK - 1) / CHUNK));
   if (c.dtype == MOE_F32)
     return launch_pdl(combine_kernel<float, KM>, grid, dim3(NT), 0, s, Y, slot_of, gate, c.T,
-                      c.k, nvec, y, b);
+                      c.k, nvec, y, b, (int64_t)max_rows(c), chk);
   return launch_pdl(combine_kernel<__nv_bfloat16, KM>, grid, dim3(NT), 0, s, Y, slot_of, gate,
-                    c.T, c.k, nvec, y, b);
+                    c.T, c.k, nvec, y, b, (int64_t)max_rows(c), chk);
 }
 
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
-                           const float* gate, void* y, cudaStream_t s, const void* base) {
+                           const float* gate, void* y, cudaStream_t s, const void* base,
+                           int32_t* chk) {
   const uint4* b = static_cast<const uint4*>(base);
   const uint4* Yv = static_cast<const uint4*>(Y);
   uint4* yv = static_cast<uint4*>(y);
-  if (c.k <= 2) return launch_combine_km<2>(c, Yv, slot_of, gate, yv, b, s);
-  if (c.k <= 4) return launch_combine_km<4>(c, Yv, slot_of, gate, yv, b, s);
-  return launch_combine_km<kMaxK>(c, Yv, slot_of, gate, yv, b, s);
+  if (c.k <= 2) return launch_combine_km<2>(c, Yv, slot_of, gate, yv, b, s, chk);
+  if (c.k <= 4) return launch_combine_km<4>(c, Yv, slot_of, gate, yv, b, s, chk);
+  return launch_combine_km<kMaxK>(c, Yv, slot_of, gate, yv, b, s, chk);
 }
 
 // off[0] = 0, off[1] = rows: the one-group offsets of the shared expert.

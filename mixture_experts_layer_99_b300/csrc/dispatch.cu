@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(1024) disp_scan_kernel(const int32_t* __restri
 __global__ void __launch_bounds__(NT) disp_assign_kernel(
     const int32_t* __restrict__ idx, int64_t nslots, int k, int E, int C,
     const int32_t* __restrict__ base, const int32_t* __restrict__ offset,
-    int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row) {
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row, int64_t rows_cap,
+    int32_t* __restrict__ chk) {
   __shared__ int wcnt[NW][kMaxE];
   __shared__ int offs[kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(NT) disp_assign_kernel(
       int32_t row = -1;
       if (valid && pos < C) {
         row = offs[e] + pos;
-        token_of_row[row] = (int32_t)(s / k);
+        if (moe_check(row < rows_cap, chk, 53)) token_of_row[row] = (int32_t)(s / k);
+        else row = -1;
       }
       slot_of[s] = row;
     }
@@ -150,12 +152,14 @@ __global__ void __launch_bounds__(NT) disp_gather_kernel(const uint4* __restrict
                                                          const int32_t* __restrict__ token_of_row,
                                                          const int32_t* __restrict__ offset,
                                                          int E, int nvec,
-                                                         uint4* __restrict__ xd) {
+                                                         uint4* __restrict__ xd, int T,
+                                                         int32_t* __restrict__ chk) {
   pdl_wait();
   const int nrows = offset[E];
   const int row = blockIdx.x * NW + (threadIdx.x >> 5);
   if (row >= nrows) return;
   const int t = token_of_row[row];
+  if (!moe_check((unsigned)t < (unsigned)T, chk, 51)) return;
   const uint4* src = x + (size_t)t * nvec;
   uint4* dst = xd + (size_t)row * nvec;
   for (int v = threadIdx.x & 31; v < nvec; v += 32) dst[v] = __ldg(src + v);
@@ -164,13 +168,14 @@ __global__ void __launch_bounds__(NT) disp_gather_kernel(const uint4* __restrict
 }  // namespace
 
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* token_of_row,
-                          const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s) {
+                          const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s,
+                          int32_t* chk) {
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   const int64_t gblk = (rows_bound + NW - 1) / NW;
   if (gblk <= 0) return cudaSuccess;
   return launch_pdl(disp_gather_kernel, dim3((unsigned)gblk), dim3(NT), 0, s,
                     static_cast<const uint4*>(x), token_of_row, offset, c.E, nvec,
-                    static_cast<uint4*>(xd));
+                    static_cast<uint4*>(xd), c.T, chk);
 }
 
 cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const void* x,
@@ -182,13 +187,13 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const voi
   disp_count_kernel<<<nblk, NT, 0, s>>>(idx, nslots, c.E, hist, hdr);
   disp_scan_kernel<<<1, 1024, 0, s>>>(hist, nblk, c.E, c.capacity, base, count, offset);
   disp_assign_kernel<<<nblk, NT, 0, s>>>(idx, nslots, c.k, c.E, c.capacity, base, offset,
-                                         slot_of, token_of_row);
+                                         slot_of, token_of_row, rows_bound, hdr);
   const int nvec = (int)((size_t)c.d * elem_bytes(c) / 16);
   const int64_t gblk = (rows_bound + NW - 1) / NW;
   if (gblk > 0)
     disp_gather_kernel<<<(unsigned)gblk, NT, 0, s>>>(static_cast<const uint4*>(x),
                                                      token_of_row, offset, c.E, nvec,
-                                                     static_cast<uint4*>(xd));
+                                                     static_cast<uint4*>(xd), c.T, hdr);
   return cudaGetLastError();
 }
 

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     int32_t* __restrict__ slot_of, int32_t* __restrict__ token_of_row,
     float* __restrict__ prob_sum, float* __restrict__ f, float* __restrict__ P,
     float* __restrict__ Lb, int32_t* __restrict__ dropped, uint4* __restrict__ zero_y,
-    int y_vec16) {
+    int y_vec16, int64_t rows_cap, int32_t* __restrict__ chk) {
   __shared__ int tot[kMaxE], base[kMaxE], offs[kMaxE + 1];
   __shared__ int wcnt[8][kMaxE];
   __shared__ float psum[kMaxE];
@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     if (in) {
       if (valid && pos < C) {
         row = offs[e] + pos;
-        token_of_row[row] = (int32_t)(s / k);
+        if (moe_check(row < rows_cap, chk, 53)) token_of_row[row] = (int32_t)(s / k);
+        else row = -1;
       }
       slot_of[s] = row;
     }
@@ -258,14 +259,16 @@ cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* id
                                         int nparts, int32_t* count, int32_t* offset,
                                         int32_t* slot_of, int32_t* token_of_row,
                                         float* prob_sum, float* f, float* P, float* Lb,
-                                        int32_t* dropped, void* zero_y, cudaStream_t s) {
+                                        int32_t* dropped, void* zero_y, cudaStream_t s,
+                                        int32_t* chk) {
   const int ntiles = router_tc_tiles(c);
   const int y_vec16 = (int)((size_t)c.d * elem_bytes(c) / 16);
   return launch_pdl(dispatch_tiles_kernel, dim3(ntiles), dim3(256), 0, s, idx, c.T, c.k, c.E,
                     c.capacity, router_tc_rows(c), tile_hist, ntiles, partial, nparts, count,
                     offset, slot_of,
                     token_of_row, prob_sum, f, P, Lb, dropped,
-                    c.k == 1 ? static_cast<uint4*>(zero_y) : (uint4*)nullptr, y_vec16);
+                    c.k == 1 ? static_cast<uint4*>(zero_y) : (uint4*)nullptr, y_vec16,
+                    max_rows(c), chk);
 }
 
 }  // namespace moe

@@ -86,6 +86,21 @@ enum HeaderWord : int {
   kHdrBytes = 256,
 };
 
+// Checked builds (-DMOE_CHECK): a kernel that indexes with data another
+// kernel wrote tests the index first; moe_check returns whether it holds and,
+// if not, records MOE_ERR_DEVICE_CHECK and the site in the status header
+// (when there is one), and the caller skips the access. Other builds compile
+// the test away (moe_check is then constantly true).
+#ifdef MOE_CHECK
+__device__ __forceinline__ bool moe_check(bool ok, int32_t* hdr, int where) {
+  if (!ok && hdr != nullptr && atomicCAS(hdr + kHdrStatus, 0, (int)MOE_ERR_DEVICE_CHECK) == 0)
+    atomicExch(hdr + kHdrWhere, where);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool moe_check(bool, int32_t*, int) { return true; }
+#endif
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline size_t elem_bytes(const moe_config_t& c) { return c.dtype == MOE_F32 ? 4 : 2; }
@@ -183,13 +198,15 @@ cudaError_t launch_dispatch(const moe_config_t& c, const int32_t* idx, const voi
                             int32_t* token_of_row, void* xd, int32_t* hist, int32_t* base,
                             int64_t rows_bound, cudaStream_t s, int32_t* hdr = nullptr);
 cudaError_t launch_gather(const moe_config_t& c, const void* x, const int32_t* token_of_row,
-                          const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s);
+                          const int32_t* offset, void* xd, int64_t rows_bound, cudaStream_t s,
+                          int32_t* chk = nullptr);
 cudaError_t launch_dispatch_from_router(const moe_config_t& c, const int32_t* idx,
                                         const int32_t* tile_hist, const float* partial,
                                         int nparts, int32_t* count, int32_t* offset,
                                         int32_t* slot_of, int32_t* token_of_row,
                                         float* prob_sum, float* f, float* P, float* Lb,
-                                        int32_t* dropped, void* zero_y, cudaStream_t s);
+                                        int32_t* dropped, void* zero_y, cudaStream_t s,
+                                        int32_t* chk = nullptr);
 cudaError_t launch_ffn(const moe_config_t& c, const void* xd, const int32_t* offset,
                        const void* W1, const void* W3, const void* W2, const void* b1,
                        const void* b2, void* Y, void* h, int64_t rows_bound, int32_t* hdr,
@@ -213,7 +230,7 @@ cudaError_t launch_ffn_tc(const moe_config_t& c, const void* xd, const int32_t* 
                           cudaStream_t s, const FfnFusion* fz = nullptr);
 cudaError_t launch_combine(const moe_config_t& c, const void* Y, const int32_t* slot_of,
                            const float* gate, void* y, cudaStream_t s,
-                           const void* base = nullptr);
+                           const void* base = nullptr, int32_t* chk = nullptr);
 cudaError_t launch_one_group_offsets(int32_t* off, int rows, cudaStream_t s);
 
 // ---- backward pass
@@ -236,13 +253,14 @@ cudaError_t launch_wgrad_tc(const void* A, int64_t lda, const void* B, int64_t l
 int bwd_wg_splits(const moe_config_t& c);
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dy, const void* Y,
                                const int32_t* slot_of, const float* gate, void* dY, float* dg,
-                               cudaStream_t s);
+                               cudaStream_t s, int32_t* chk = nullptr);
 cudaError_t launch_bwd_router(const moe_config_t& c, const float* logits, const int32_t* idx,
                               const float* gate, const float* dg, const float* f, float alpha,
                               float* dz, void* dz_bf16, int Kp, cudaStream_t s);
 int bwd_wg_group_tokens(const moe_config_t& c);
 cudaError_t launch_bwd_dx(const moe_config_t& c, const void* dxd, const int32_t* slot_of,
-                          const void* dxr, void* dx, cudaStream_t s, const void* dxs = nullptr);
+                          const void* dxr, void* dx, cudaStream_t s, const void* dxs = nullptr,
+                          int32_t* chk = nullptr);
 cudaError_t launch_bwd_wg(const moe_config_t& c, const float* dz, const void* dzb, int Kp,
                           const void* x, int32_t* goff, float* part, float* dWg, float* dbias,
                           int32_t* hdr, cudaStream_t s);

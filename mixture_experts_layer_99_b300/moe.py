@@ -18,12 +18,17 @@ from typing import Optional
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300.so")
+# MOE_B300_CHECKED=1 loads the checked build (index checks in the kernels,
+# MOE_ERR_DEVICE_CHECK on a failure; the same ABI)
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libmoe_b300_check.so" if os.environ.get("MOE_B300_CHECKED") == "1"
+                        else "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
-          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT"}
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+          6: "MOE_ERR_DEVICE_CHECK"}
 
 EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspace_size",
             "moe_workspace_size_host", "moe_workspace_init", "moe_device_status",

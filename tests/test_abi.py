@@ -32,6 +32,22 @@ def test_library_exports_every_declared_symbol():
     assert set(moe.EXPORTED) <= syms
 
 
+def test_checked_library_exports_the_same_symbols():
+    """The checked build (index checks in the kernels) has the same ABI."""
+    import ctypes as ct
+    from mixture_experts_layer_99_b300 import build as B
+    if not os.path.exists(B.LIB_CHECK):
+        B.build(check=True)
+    L = ct.CDLL(B.LIB_CHECK)
+    for s in sorted(declared_symbols()):
+        assert hasattr(L, s), s
+    L.moe_abi_version.restype = ct.c_int32
+    assert L.moe_abi_version() == moe.lib().moe_abi_version()
+    L.moe_status_string.restype = ct.c_char_p
+    L.moe_status_string.argtypes = [ct.c_int32]
+    assert b"check" in L.moe_status_string(6)
+
+
 def test_abi_version_and_status_strings():
     L = moe.lib()
     # 1.01: moe_config_t carries noise_scale (std-scaled router noise);
