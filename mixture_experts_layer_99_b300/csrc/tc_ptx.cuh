@@ -118,6 +118,11 @@ __device__ __forceinline__ void bulk_wait0() {
 }
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
+// Generic-proxy writes (any state space, another CTA's accesses included)
+// before later async-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
