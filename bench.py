@@ -520,11 +520,14 @@ def main():
 
     # ---- end to end through the host-buffer C call (pinned host x and y):
     # every step copies its tokens in, runs the layer and copies y (and
-    # L_balance) out; steps alternate between two streams, each with its own
-    # workspace and output buffer, so one step's copies overlap the other's
-    # compute, as a serving loop would run them
-    e2e_streams = [stream, torch.cuda.Stream(dev)]
+    # L_balance) out, through moe_layer_forward_host_pipelined as a serving
+    # loop would run it: copies in, layers and copies out on three streams,
+    # two workspaces (each with its three events) taken in turn, so one
+    # step's copies overlap the neighbouring steps' layers while the layers
+    # run one after another
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     e2e_ws = [ws, moe.workspace(cfg, dev, host_io=True)]
+    e2e_ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
     xh = [s["x"].cpu().pin_memory() for s in sets[:2]]
     yh = [torch.empty_like(xh[0]).pin_memory() for _ in range(2)]
     Lh = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -532,25 +535,41 @@ def main():
 
     def e2e_step(i):
         j = i % 2
-        with torch.cuda.stream(e2e_streams[j]):
-            moe.layer_forward_host(cfg, xh[i % 2], sets[i % nsets], yh[j], ws=e2e_ws[j],
-                                   L_host=Lh[j])
+        moe.layer_forward_host_pipelined(cfg, xh[i % 2], sets[i % nsets], yh[j], ws=e2e_ws[j],
+                                         events=e2e_ev[j], copy_in=s_in, compute=stream,
+                                         copy_out=s_out, L_host=Lh[j])
 
-    for i in range(4):
+    # the same steady state as the timed device steps: about 1 s of untimed
+    # steps first, clocks sampled during the timed ones
+    e2e_clocks = ClockSampler(local_rank) if rank == 0 else None
+    if e2e_clocks:
+        e2e_clocks.start()
+    t_warm = time.time() + 1.0
+    i = 0
+    while time.time() < t_warm or i < 4:
         e2e_step(i)
+        i += 1
+        if i % 8 == 0:
+            s_out.synchronize()
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(e2e_streams[0])
-    e2e_streams[1].wait_event(a)
+    if e2e_clocks:
+        e2e_clocks.mark("start")
+    a.record(stream)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
     for i in range(e2e_steps):
         e2e_step(i)
-    done1 = torch.cuda.Event()
-    done1.record(e2e_streams[1])
-    e2e_streams[0].wait_event(done1)
-    b.record(e2e_streams[0])
+    done = torch.cuda.Event()
+    done.record(s_out)
+    stream.wait_event(done)
+    b.record(stream)
     torch.cuda.synchronize(dev)
+    if e2e_clocks:
+        e2e_clocks.mark("end")
+    e2e_clk = e2e_clocks.stop() if e2e_clocks else None
     e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, pg, dev)
     bytes_x = cfg.T * cfg.d * sets[0]["x"].element_size()
 
@@ -615,7 +634,8 @@ def main():
             cpu_baseline=cpu,
             e2e=dict(value=w.T * world / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=bytes_x,
                      d2h_bytes_per_step=bytes_x + 4, ms_per_step=e2e_ms,
-                     call="moe_layer_forward_host, steps alternating over two streams"),
+                     call="moe_layer_forward_host_pipelined: copies in, layers and copies out on three streams, two workspaces in turn",
+                     clocks=e2e_clk),
             gpu_launches=moe.lib().moe_layer_forward_launch_count(moe.ctypes.byref(cfg))
             * args.steps,
             clocks=clk,

@@ -73,6 +73,7 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st *moe_stream_t; /* the same handle as cudaStream_t */
+typedef struct CUevent_st *moe_event_t;   /* the same handle as cudaEvent_t */
 
 typedef enum {
   MOE_OK = 0,
@@ -411,6 +412,23 @@ MOE_API moe_status_t moe_layer_forward_host(const moe_config_t *cfg, const void 
                                     const moe_layer_inputs_t *in, void *y_host,
                                     float *L_balance_host, void *ws, size_t ws_bytes,
                                     moe_stream_t stream);
+
+/* moe_layer_forward_host for a stream of calls (a serving loop): the copy in
+ * runs on copy_in, the layer on compute, the copies out on copy_out, so that
+ * one call's copies overlap other calls' layers while the layers themselves
+ * run one after another on compute. ev[3] are three events the caller
+ * created for this workspace and passes to every call with it; they order
+ * the calls that share the workspace (its staging buffers): a call's copy in
+ * waits until the previous call with this ws has finished its layer (ev[1]),
+ * and its layer waits for its copy in (ev[0]) and for the previous call's
+ * copy out (ev[2]). Alternate two workspaces (each with its own events) to
+ * overlap consecutive calls. The caller synchronises copy_out (or waits on
+ * ev[2]) before reading y_host. Same workspace size as
+ * moe_layer_forward_host. */
+MOE_API moe_status_t moe_layer_forward_host_pipelined(
+    const moe_config_t *cfg, const void *x_host, const moe_layer_inputs_t *in, void *y_host,
+    float *L_balance_host, void *ws, size_t ws_bytes, moe_stream_t copy_in, moe_stream_t compute,
+    moe_stream_t copy_out, const moe_event_t *ev);
 
 #ifdef __cplusplus
 }

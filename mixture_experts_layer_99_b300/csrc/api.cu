@@ -477,6 +477,45 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* x_host,
   return MOE_OK;
 }
 
+moe_status_t moe_layer_forward_host_pipelined(const moe_config_t* cfg, const void* x_host,
+                                              const moe_layer_inputs_t* in, void* y_host,
+                                              float* L_balance_host, void* ws, size_t ws_bytes,
+                                              moe_stream_t copy_in, moe_stream_t compute,
+                                              moe_stream_t copy_out, const moe_event_t* ev) {
+  moe_status_t st = validate(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_layer_inputs(cfg, in)) != MOE_OK) return st;
+  if (!x_host || !y_host || !ev || !ev[0] || !ev[1] || !ev[2]) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*cfg, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total_host)) != MOE_OK) return st;
+  cudaStream_t si = (cudaStream_t)copy_in, sc = (cudaStream_t)compute,
+               so = (cudaStream_t)copy_out;
+  cudaEvent_t in_done = (cudaEvent_t)ev[0], layer_done = (cudaEvent_t)ev[1],
+              out_done = (cudaEvent_t)ev[2];
+  const size_t bytes = (size_t)cfg->T * cfg->d * elem_bytes(*cfg);
+  void* xs = at<void>(ws, L.x_stage);
+  void* ys = at<void>(ws, L.y_stage);
+  // x_stage is free once the previous call with this ws finished its layer
+  // (waiting on an event that was never recorded does not wait)
+  if (cudaStreamWaitEvent(si, layer_done, 0) != cudaSuccess ||
+      cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, si) != cudaSuccess ||
+      cudaEventRecord(in_done, si) != cudaSuccess ||
+      cudaStreamWaitEvent(sc, in_done, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(sc, out_done, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = layer_forward_impl(cfg, xs, in, nullptr, ys, nullptr, ws, sc);
+  if (st != MOE_OK) return st;
+  if (cudaEventRecord(layer_done, sc) != cudaSuccess ||
+      cudaStreamWaitEvent(so, layer_done, 0) != cudaSuccess ||
+      cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (L_balance_host &&
+      cudaMemcpyAsync(L_balance_host, at<float>(ws, L.L), sizeof(float),
+                      cudaMemcpyDeviceToHost, so) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cudaEventRecord(out_done, so) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {

@@ -34,6 +34,7 @@ EXPORTED = ["moe_abi_version", "moe_status_string", "moe_capacity", "moe_workspa
             "moe_workspace_size_host", "moe_workspace_init", "moe_device_status",
             "moe_router_topk", "moe_dispatch", "moe_expert_ffn", "moe_combine",
             "moe_aux_stats", "moe_layer_forward", "moe_layer_forward_host",
+            "moe_layer_forward_host_pipelined",
             "moe_layer_forward_launch_count", "moe_layer_forward_profiled",
             "moe_workspace_size_shared", "moe_layer_forward_shared", "moe_dispatch_static_scratch",
             "moe_workspace_size_backward", "moe_layer_backward",
@@ -129,6 +130,9 @@ def lib():
                                                  POINTER(c_void_p)]),
         "moe_layer_forward_host": (c_int32, [cfgp, vp, POINTER(LayerInputs), vp, vp, vp,
                                              c_size_t, vp]),
+        "moe_layer_forward_host_pipelined": (c_int32, [cfgp, vp, POINTER(LayerInputs), vp, vp,
+                                                       vp, c_size_t, vp, vp, vp,
+                                                       POINTER(c_void_p)]),
         "moe_workspace_size_backward": (c_int32, [cfgp, POINTER(c_size_t)]),
         "moe_layer_backward": (c_int32, [cfgp, POINTER(LayerInputs), POINTER(LayerOutputs), vp,
                                          ctypes.c_float, POINTER(LayerGrads), vp, c_size_t, vp,
@@ -426,6 +430,28 @@ def layer_forward_host(cfg, x_host, weights: dict, y_host, *, ws, L_host=None):
     _need(y_host, "y_host", _dt(cfg), (cfg.T, cfg.d), torch.device("cpu"))
     _call("moe_layer_forward_host", ctypes.byref(cfg), _ptr(x_host), ctypes.byref(li),
           _ptr(y_host), _ptr(L_host), _ptr(ws), ws.numel(), _stream(dev))
+
+
+def layer_forward_host_pipelined(cfg, x_host, weights: dict, y_host, *, ws, events,
+                                 copy_in, compute, copy_out, L_host=None):
+    """moe_layer_forward_host_pipelined: the copy in on ``copy_in``, the layer
+    on ``compute``, the copies out on ``copy_out`` (torch.cuda.Stream each);
+    ``events`` are three torch.cuda.Event objects that belong to ``ws`` and
+    go with it to every call. Synchronise ``copy_out`` (or wait on
+    events[2]) before reading y_host."""
+    dev = weights["Wg"].device
+    li = _layer_inputs(cfg, weights, dev, with_x=False)
+    _need(x_host, "x_host", _dt(cfg), (cfg.T, cfg.d), torch.device("cpu"))
+    _need(y_host, "y_host", _dt(cfg), (cfg.T, cfg.d), torch.device("cpu"))
+    if len(events) != 3:
+        raise ValueError("three events per workspace")
+    for e in events:  # torch creates the CUDA event on its first record
+        if not e.cuda_event:
+            e.record(compute)
+    evs = (c_void_p * 3)(*[c_void_p(e.cuda_event) for e in events])
+    _call("moe_layer_forward_host_pipelined", ctypes.byref(cfg), _ptr(x_host), ctypes.byref(li),
+          _ptr(y_host), _ptr(L_host), _ptr(ws), ws.numel(), c_void_p(copy_in.cuda_stream),
+          c_void_p(compute.cuda_stream), c_void_p(copy_out.cuda_stream), evs)
 
 
 def workspace_backward(cfg: Config, device="cuda") -> torch.Tensor:

@@ -150,6 +150,13 @@ def test_null_pointers_rejected_before_any_launch():
     out = moe.LayerOutputs(*([4096] + [None] * 10))
     assert L.moe_layer_forward(r, ctypes.byref(inp), ctypes.byref(out), fake, 1 << 30,
                                None) == 1
+    # the pipelined host call needs its three events
+    full = moe.LayerInputs(None, 4096, None, None, 4096, None, 4096, None, None)
+    no_ev = (ctypes.c_void_p * 3)(None, None, None)
+    assert L.moe_layer_forward_host_pipelined(r, fake, ctypes.byref(full), fake, None, fake,
+                                              1 << 30, None, None, None, no_ev) == 1
+    assert L.moe_layer_forward_host_pipelined(r, fake, ctypes.byref(full), fake, None, fake,
+                                              1 << 30, None, None, None, None) == 1
 
 
 def test_workspace_checks():

@@ -103,6 +103,39 @@ def test_layer_host_io_matches_device_call():
     assert Lh.item() == out["L_balance"].item()
 
 
+@pytest.mark.parametrize("name", ["switch_top1", "longtail"])
+def test_pipelined_host_calls_match_device_calls(name):
+    """moe_layer_forward_host_pipelined over six calls on two workspaces and
+    three streams, with different inputs per call: each call's y and
+    L_balance equal those of the device call on the same inputs, so the
+    events keep every staging buffer from being reused too early."""
+    w = W.small(WL[name], T=700, d=128, H=256)
+    cfg = moe.config_from_workload(w)
+    sets = [W.make_inputs(w, seed=s) for s in range(3)]
+    dsets = [W.to_device(s, DEV) for s in sets]
+    ref = [moe.layer_forward(cfg, d) for d in dsets]
+    torch.cuda.synchronize()
+    wss = [moe.workspace(cfg, DEV, host_io=True) for _ in range(2)]
+    evs = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
+    s_in, s_c, s_out = (torch.cuda.Stream() for _ in range(3))
+    xh = [s["x"].pin_memory() for s in sets]
+    n = 6
+    yh = [torch.empty_like(xh[0]).pin_memory() for _ in range(n)]
+    Lh = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(n)]
+    for i in range(n):
+        j = i % 3
+        moe.layer_forward_host_pipelined(cfg, xh[j], dsets[j], yh[i], ws=wss[i % 2],
+                                         events=evs[i % 2], copy_in=s_in, compute=s_c,
+                                         copy_out=s_out, L_host=Lh[i])
+    s_out.synchronize()
+    torch.cuda.synchronize()
+    for i in range(n):
+        assert torch.equal(yh[i], ref[i % 3]["y"].cpu()), i
+        assert Lh[i].item() == ref[i % 3]["L_balance"].item(), i
+    for ws in wss:
+        assert moe.device_status(ws) == (0, 0)
+
+
 def test_layer_deterministic():
     w = W.small(WL["longtail"], T=3000, d=128, H=128)
     cfg = moe.config_from_workload(w)
