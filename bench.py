@@ -271,7 +271,7 @@ def time_oracle(w, target_s=12.0, seed=0):
 
     n = min(w.T, 64)
     t = run(n)
-    while t < target_s / 4 and n < w.T:
+    while t < target_s / 2 and n < w.T:
         n = min(w.T, max(n * 2, int(n * target_s / max(t, 1e-3) / 2)))
         t = run(n)
     return dict(value=n / t, unit=UNIT, cores=cores, kind="oracle",
@@ -388,6 +388,52 @@ def stage_times(moe, cfg, sets, nsets, ws, out, stream, dev, want):
             moe.layer_forward_profiled(cfg, sets[i % nsets], evs[i], ws=ws, out=out)
         torch.cuda.synchronize(dev)
         return _stage_avg(evs), f"eager moe_layer_forward_profiled calls ({exc.__class__.__name__})"
+
+
+def router_context(moe, cfg, sets, nsets, ws, out, stream, dev, reps=4):
+    """The router step on its own, to read its stage time inside the layer:
+    CUDA-graph replays of M moe_router_topk calls over the rotating input sets
+    (the router kernel and the small kernel that sums its probability
+    partials), each between two event nodes, (a) alone, (b) right after a
+    memset of the layer's output y (T x d), which leaves y's lines dirty in
+    L2 as the previous layer call's combine does, so that the router's loads
+    also carry their write-back, and (c) two event nodes with nothing
+    between them (the floor of one event-pair measurement). Medians in ms."""
+    M = 8
+
+    def med(kind):
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(M)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(M):
+                s = sets[i % nsets]
+                if kind == "after_write":
+                    out["y"].zero_()
+                evs[i][0].record(stream)
+                if kind != "floor":
+                    moe.router_topk(cfg, s["x"], s["Wg"], s.get("bias"), s.get("noise"),
+                                    ws=ws, logits=True)
+                evs[i][1].record(stream)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize(dev)
+            ts += [r[0].elapsed_time(r[1]) for r in evs]
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    try:
+        return {k: med(k) for k in ("alone", "after_write", "floor")}
+    except Exception:  # pragma: no cover - capture not available
+        torch.cuda.synchronize(dev)
+        return None
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -517,6 +563,8 @@ def main():
     # which records CUDA events on this stream at the stage boundaries
     st, stage_how = stage_times(moe, cfg, sets, nsets, ws, out, stream, dev,
                                 max(10, min(args.steps, 200)))
+    rctx = (router_context(moe, cfg, sets, nsets, ws, out, stream, dev)
+            if work["tc_router"] else None)
 
     # ---- end to end through the host-buffer C call (pinned host x and y):
     # every step copies its tokens in, runs the layer and copies y (and
@@ -653,10 +701,18 @@ def main():
                 gemm_frac_nominal_dense=achieved / NOMINAL_BF16_TFLOPS,
                 gemm_weight_gbs=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9,
                 gemm_weight_hbm_frac=work["gemm_bytes"] / (gemm_ms / 1e3) / 1e9 / hbm,
+                router_context_ms=rctx,
+                router_alone_gbs=(None if not rctx
+                                  else work["router_bytes"] / (rctx["alone"] / 1e3) / 1e9),
+                router_alone_hbm_frac=(None if not rctx else
+                                       work["router_bytes"] / (rctx["alone"] / 1e3) / 1e9 / hbm),
                 hbm_peak_gbs=hbm,
                 bytes=dict(router=work["router_bytes"], dispatch=work["dispatch_bytes"],
                            combine=work["combine_bytes"], gemm=work["gemm_bytes"]),
-                note=(f"stage times from {stage_how}; dispatch = per-tile dispatch + gather "
+                note=(f"stage times from {stage_how}; router_context_ms: moe_router_topk "
+                      f"alone, after a memset of y (the previous call's output lines dirty in "
+                      f"L2, as after a combine), and an empty event pair, each between event "
+                      f"nodes of a CUDA graph; dispatch = per-tile dispatch + gather "
                       f"launches; " + ("for k = 1 the combine runs inside GEMM2 (no combine "
                                        "stage)" if comb_ms is None else
                                        "combine = the combine launch"))),

@@ -164,7 +164,11 @@ __device__ __forceinline__ void router_tile_epilogue(
   const int t = tile * tile_rows + r;
   const bool valid = r < tile_rows && t < T;
   const int e0 = p * Q;
-  const bool vec4 = (E & 3) == 0;  // rows of [T, E] fp32 arrays are 16-byte aligned
+  // 16-byte vectors along rows of the [T, E] fp32 arrays when every row starts
+  // on a 16-byte boundary
+  const bool rows16 = (E & 3) == 0;
+  const bool vec4n = rows16 && (reinterpret_cast<uintptr_t>(noise) & 15u) == 0;
+  const bool vec4l = rows16 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   // selection keys l = (z + b + s g) / tau (one reciprocal; tau = 1 leaves them as they are)
   if (valid && bias) {
 #pragma unroll
@@ -196,7 +200,7 @@ __device__ __forceinline__ void router_tile_epilogue(
   if (valid) {
     if (noise) {
       const float* nr = noise + (size_t)t * E + e0;
-      if (vec4) {
+      if (vec4n) {
 #pragma unroll
         for (int q = 0; q < Q; q += 4) {
           if (e0 + q < E) {
@@ -229,7 +233,7 @@ __device__ __forceinline__ void router_tile_epilogue(
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   if (valid && logits) {
     float* lr = logits + (size_t)t * E + e0;
-    if (vec4) {
+    if (vec4l) {
 #pragma unroll
       for (int q = 0; q < Q; q += 4)
         if (e0 + q < E) *reinterpret_cast<float4*>(lr + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
