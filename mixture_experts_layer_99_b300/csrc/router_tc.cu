@@ -15,11 +15,11 @@
 // step into a TMEM accumulator row per token.
 //   warp 0       TMA producer (x tile [128 x 64] + Wg tile [E_pad x 64])
 //   warp 1       TMEM owner, MMA issuer
-//   warps 2-17   epilogue, four threads per token: warps 2-5 move the
-//                tile's logits from TMEM to shared memory (one row per
-//                token), then each token's four threads take a quarter of
-//                its experts each and combine max, top-k and the softmax sum
-//                with shuffles
+//   warps 2-17   epilogue, four threads per token: EP/16 groups of four warps
+//                move the tile's logits from TMEM to shared memory (one row
+//                per token; each group 16 of the EP columns), then each
+//                token's four threads take a quarter of its experts each and
+//                combine max, top-k and the softmax sum with shuffles
 // When the batch has few 128-token tiles (e.g. a decode step of 64 tokens),
 // the K range of each tile is split over a cluster of CTAs (SPLIT): each
 // leaves its fp32 partial logits in its shared memory, and the cluster's
@@ -57,6 +57,7 @@ constexpr int LPAD = 4;
 template <int EP>
 struct EpiSmem {
   alignas(16) float L[BM][EP + LPAD];
+  alignas(16) float bias[EP];  // the router bias (0 past E, or without one)
   float part[EP];
   int hist[EP];
 };
@@ -106,27 +107,6 @@ __device__ __forceinline__ bool epi_bar_or(bool fail) {
   return r != 0;
 }
 
-template <int EP>
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[EP]) {
-  static_assert(EP % 16 == 0, "EP multiple of 16");
-#pragma unroll
-  for (int c = 0; c < EP; c += 32) {
-    if (c + 32 <= EP) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[c + j] = __uint_as_float(r[j]);
-    } else {
-      uint32_t r[16];
-      tmem_ld16(taddr + c, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[c + j] = __uint_as_float(r[j]);
-    }
-  }
-}
-
 // Thread p's quarter of token r's row of the scratch (Q = EP/4 floats, a
 // multiple of 4).
 template <int EP>
@@ -152,10 +132,11 @@ __device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi)
 // One token's four threads (lanes 4j..4j+3 of a warp; thread p owns experts
 // [p Q, p Q + Q), Q = EP/4): keys, softmax, top-k (descending, ties to the
 // lower index), gates, and the tile's per-expert selection counts and sums of
-// p (fixed order). v holds the thread's Q raw logits on entry.
+// p (fixed order). v holds the thread's Q raw logits on entry, or z + b + g
+// when keys_done (the copy out of TMEM added bias and noise already).
 template <int EP, int KM>
 __device__ __forceinline__ void router_tile_epilogue(
-    float (&v)[EP / TPT], int tile, int tile_rows, int r, int p, int etid,
+    float (&v)[EP / TPT], bool keys_done, int tile, int tile_rows, int r, int p, int etid,
     const float* __restrict__ bias,
     const float* __restrict__ noise, float noise_scale, float tau, int T, int E, int k,
     float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate,
@@ -170,10 +151,16 @@ __device__ __forceinline__ void router_tile_epilogue(
   const bool vec4n = rows16 && (reinterpret_cast<uintptr_t>(noise) & 15u) == 0;
   const bool vec4l = rows16 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   // selection keys l = (z + b + s g) / tau (one reciprocal; tau = 1 leaves them as they are)
-  if (valid && bias) {
+  if (valid && bias && !keys_done) {
+    const float4* br = reinterpret_cast<const float4*>(&es.bias[e0]);
 #pragma unroll
-    for (int q = 0; q < Q; ++q)
-      if (e0 + q < E) v[q] += __ldg(bias + e0 + q);
+    for (int q = 0; q < Q; q += 4) {
+      const float4 b4 = br[q / 4];
+      v[q] += b4.x;
+      v[q + 1] += b4.y;
+      v[q + 2] += b4.z;
+      v[q + 3] += b4.w;
+    }
   }
   // noise strength: 1, or noise_scale times the population standard deviation
   // of the token's E logits (z + b), summed by the token's four threads in a
@@ -198,7 +185,7 @@ __device__ __forceinline__ void router_tile_epilogue(
     sn = noise_scale * sqrtf(s2 / (float)E);
   }
   if (valid) {
-    if (noise) {
+    if (noise && !keys_done) {
       const float* nr = noise + (size_t)t * E + e0;
       if (vec4n) {
 #pragma unroll
@@ -339,14 +326,19 @@ __device__ __forceinline__ void router_tile_epilogue(
     }
   }
   epi_bar();  // probabilities and counts of the whole tile are in place
-  // per-expert sums over the tile's 128 tokens: eight threads per expert each
-  // walk 16 rows in token order, then a fixed butterfly adds the eight
+  // per-expert sums over the tile's 128 tokens: eight threads per expert,
+  // thread q8 adding rows q8, q8 + 8, ..., q8 + 120 in that order, then a
+  // fixed butterfly adds the eight. Eight rows apart, the row stride (EP + 4
+  // floats) advances the bank by a multiple of 32, and rows q8 = 0..7 start
+  // on eight different banks, so a warp's four experts x eight threads read
+  // 32 different banks (rows 16 apart, as before, put all eight threads of an
+  // expert on one bank).
   {
     const int e = etid >> 3, q8 = etid & 7;
     float a = 0.f;
     if (e < E) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) a += es.L[16 * q8 + i][e];
+      for (int i = 0; i < 16; ++i) a += es.L[q8 + 8 * i][e];
     }
     a += __shfl_xor_sync(0xffffffffu, a, 1);
     a += __shfl_xor_sync(0xffffffffu, a, 2);
@@ -386,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&st.tmem_full[a], 1);
-      mbar_init(&st.tmem_empty[a], 128);
+      mbar_init(&st.tmem_empty[a], 32 * 4 * (EP / 16));  // every TMEM-reading thread
     }
     mbar_init(&st.final_bar, 1);
     st.abort_flag = 0;
@@ -405,6 +397,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   pdl_wait();
+  // the bias may come from the previous kernel: read it after the wait, by
+  // epilogue threads (their first named barrier orders these stores before
+  // the epilogue's reads)
+  if (tid >= 64)
+    for (int e = tid - 64; e < EP; e += EPI_THREADS) st.epi.bias[e] = (bias && e < E) ? bias[e] : 0.f;
   const uint32_t tmem_base = st.tmem_base;
   // work unit u = (tile, split): K blocks [split * kb_per_split, ...) of the tile
   const int ntiles = (T + tile_rows - 1) / tile_rows;
@@ -507,32 +504,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2-5 read TMEM (thread = token row);
-    // epilogue thread etid works on token etid / 4, experts quarter etid % 4
+    // ---------------- epilogue: warps 2 + 4 g .. 5 + 4 g read columns
+    // [16 g, 16 g + 16) of the accumulator from TMEM (thread = token row;
+    // g < EP/16, so up to all 16 warps share the copy); then epilogue thread
+    // etid works on token etid / 4, experts quarter etid % 4
     constexpr int Q = EP / TPT;
     const int etid = tid - 64;  // 0..511
-    const bool tmem_warp = warp < 6;
-    const int quarter = warp & 3;
+    const int cgrp = (warp - 2) >> 2;  // column group of a TMEM warp
+    const bool tmem_warp = cgrp < EP / 16;
+    const int quarter = warp & 3;  // a warp reads TMEM lanes 32 (warp % 4) ..
     const int lr = quarter * 32 + lane;  // the TMEM lane (token row) a TMEM warp reads
     const int r = etid >> 2, p = etid & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // With whole logits in TMEM (no split) and noise added as given (not
+    // std-scaled), the copy out of TMEM adds bias and noise: each thread
+    // loads its 16 noise values before it waits for the tile's accumulator,
+    // so that their DRAM latency passes under the tile's x stream instead of
+    // after its last MMA. Same arithmetic as the per-token epilogue: (z + b) + g.
+    const bool keys_early = !SPLIT && !(noise && noise_scale > 0.f);
+    const int c0 = 16 * cgrp;  // this TMEM warp's first column
+    const bool nvec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(noise) & 15u) == 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       const int tile = u / ksplit;
       bool fail = false;
       if (tmem_warp) {
+        const int t = tile * tile_rows + lr;
+        const bool valid = lr < tile_rows && t < T;
+        float nz[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) nz[j] = 0.f;
+        if (keys_early && noise && valid) {
+          const float* nr = noise + (size_t)t * E + c0;
+          if (nvec) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              if (c0 + j < E) {
+                const float4 w4 = __ldg(reinterpret_cast<const float4*>(nr + j));
+                nz[j] = w4.x;
+                nz[j + 1] = w4.y;
+                nz[j + 2] = w4.z;
+                nz[j + 3] = w4.w;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < E) nz[j] = __ldg(nr + j);
+          }
+        }
         if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) {
           fail = true;
         } else {
           tc_fence_after();
-          float v[EP];
-          tmem_ld_row<EP>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * EP), v);
+          uint32_t v[16];
+          tmem_ld16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * EP + c0), v);
+          tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&st.tmem_empty[acc]);
-          // the token's (partial) logits, one row of the scratch
-          float4* row = reinterpret_cast<float4*>(&st.epi.L[lr][0]);
+          float f[16];
 #pragma unroll
-          for (int e = 0; e < EP; e += 4) row[e / 4] = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+          if (keys_early && valid) {
+            if (bias) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] += st.epi.bias[c0 + j];
+            }
+            if (noise) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] += nz[j];
+            }
+          }
+          // 16 of the token's (partial) logits or keys, into its row of the scratch
+          float4* row = reinterpret_cast<float4*>(&st.epi.L[lr][c0]);
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) row[e / 4] = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
         }
         if (++acc == 2) {
           acc = 0;
@@ -544,8 +590,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!SPLIT) {
         float v[Q];
         load_quarter<EP>(st.epi, r, p, v);
-        router_tile_epilogue<EP, KM>(v, tile, tile_rows, r, p, etid, bias, noise, noise_scale,
-                                     tau, T, E, k, logits, idx, gate, tile_hist, st.epi);
+        router_tile_epilogue<EP, KM>(v, keys_early, tile, tile_rows, r, p, etid, bias, noise,
+                                     noise_scale, tau, T, E, k, logits, idx, gate, tile_hist,
+                                     st.epi);
       }
     }
     if (!SPLIT)
@@ -601,8 +648,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       load_quarter<EP>(st.epi, r, p, v);
       if (etid < EP) st.epi.hist[etid] = 0;
       epi_bar();  // counts zeroed before the epilogue's atomics
-      router_tile_epilogue<EP, KM>(v, tile, BM, r, p, etid, bias, noise, noise_scale, tau, T, E,
-                                   k, logits, idx, gate, tile_hist, st.epi);
+      router_tile_epilogue<EP, KM>(v, false, tile, BM, r, p, etid, bias, noise, noise_scale, tau,
+                                   T, E, k, logits, idx, gate, tile_hist, st.epi);
       for (int e = etid; e < E; e += EPI_THREADS) partial[(size_t)tile * E + e] = st.epi.part[e];
     }
   }
