@@ -32,6 +32,19 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found")
 
 
+def stale(lib: str) -> bool:
+    """True if ``lib`` is missing or older than any CUDA source or header."""
+    if not os.path.exists(lib):
+        return True
+    t = os.path.getmtime(lib)
+    inc = os.path.join(HERE, "..", "include")
+    for d in (CSRC, inc):
+        for f in os.listdir(d):
+            if os.path.getmtime(os.path.join(d, f)) > t:
+                return True
+    return False
+
+
 def build(verbose: bool = False, extra: list[str] | None = None, check: bool = False) -> str:
     """Compile every source to an object file (in parallel, one nvcc per
     file, objects under _build/ or _build_check/ beside the sources) and link

@@ -124,6 +124,22 @@ __device__ __forceinline__ void load_quarter(const EpiSmem<EP>& es, int r, int p
   }
 }
 
+// Read-only loads issued where they stand: volatile asm stays in program
+// order with the mbarrier waits (also volatile asm), so a load placed before
+// a wait is in flight while the thread waits.
+__device__ __forceinline__ float4 ld_nc_early_v4(const float* p) {
+  float4 r;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float ld_nc_early(const float* p) {
+  float r;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+
 // (value, expert) a ranks before b: larger value, ties to the lower index.
 __device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
@@ -213,11 +229,6 @@ __device__ __forceinline__ void router_tile_epilogue(
 #pragma unroll
   for (int q = 0; q < Q; ++q)
     if (e0 + q >= E) v[q] = -INFINITY;
-  float m = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < Q; ++q) m = fmaxf(m, v[q]);
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   if (valid && logits) {
     float* lr = logits + (size_t)t * E + e0;
     if (vec4l) {
@@ -238,19 +249,38 @@ __device__ __forceinline__ void router_tile_epilogue(
     sv[j] = -INFINITY;
     si[j] = 0x7fffffff;
   }
+  if constexpr (KM == 2) {
+    // one pass keeping the best two: the experts come in ascending index
+    // order, so a later one ranks before a kept one only if strictly larger
+    // (a tie keeps the lower index ahead)
 #pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    float cv = v[q];
-    int ci = e0 + q;
+    for (int q = 0; q < Q; ++q) {
+      const float cv = v[q];
+      if (cv > sv[0]) {
+        sv[1] = sv[0];
+        si[1] = si[0];
+        sv[0] = cv;
+        si[0] = e0 + q;
+      } else if (cv > sv[1]) {
+        sv[1] = cv;
+        si[1] = e0 + q;
+      }
+    }
+  } else {
 #pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      if (ranks_before(cv, ci, sv[j], si[j])) {
-        const float tv = sv[j];
-        const int ti = si[j];
-        sv[j] = cv;
-        si[j] = ci;
-        cv = tv;
-        ci = ti;
+    for (int q = 0; q < Q; ++q) {
+      float cv = v[q];
+      int ci = e0 + q;
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        if (ranks_before(cv, ci, sv[j], si[j])) {
+          const float tv = sv[j];
+          const int ti = si[j];
+          sv[j] = cv;
+          si[j] = ci;
+          cv = tv;
+          ci = ti;
+        }
       }
     }
   }
@@ -288,6 +318,8 @@ __device__ __forceinline__ void router_tile_epilogue(
       }
     }
   }
+  // the token's largest key heads the merged list
+  const float m = sv[0];
   // probabilities for the statistics P_i, back into the token's row
   {
     float sum = 0.f;
@@ -540,7 +572,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
               if (c0 + j < E) {
-                const float4 w4 = __ldg(reinterpret_cast<const float4*>(nr + j));
+                const float4 w4 = ld_nc_early_v4(nr + j);
                 nz[j] = w4.x;
                 nz[j + 1] = w4.y;
                 nz[j + 2] = w4.z;
@@ -550,7 +582,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c0 + j < E) nz[j] = __ldg(nr + j);
+              if (c0 + j < E) nz[j] = ld_nc_early(nr + j);
           }
         }
         if (!mbar_wait(&st.tmem_full[acc], acc_phase, abort_flag, hdr, 14)) {
@@ -567,8 +599,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
           if (keys_early && valid) {
             if (bias) {
+              const float4* b4 = reinterpret_cast<const float4*>(&st.epi.bias[c0]);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) f[j] += st.epi.bias[c0 + j];
+              for (int j = 0; j < 16; j += 4) {
+                const float4 b = b4[j / 4];
+                f[j] += b.x;
+                f[j + 1] += b.y;
+                f[j + 2] += b.z;
+                f[j + 3] += b.w;
+              }
             }
             if (noise) {
 #pragma unroll

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def _child(*args):
-    if not os.path.exists(B.LIB_CHECK):
+    if B.stale(B.LIB_CHECK):   # missing, or built before the current sources
         B.build(check=True)
     env = dict(os.environ, MOE_B300_CHECKED="1")
     r = subprocess.run([sys.executable, os.path.join(HERE, "checked_cases.py"), *args],
