@@ -41,7 +41,32 @@ ROUTER_CASES = {
         noise="gaussian_std", noise_std=0.2),
     "std_noise_E100": W.small(WL["switch_top1"], T=200, d=64, H=64, E=100, k=2).with_(
         noise="gaussian_std", noise_std=0.5),
+    # keys formed while the accumulator leaves TMEM: bias only, noise only,
+    # and an E that is not a multiple of 4 (scalar noise loads), over tiles
+    # of one and of several column groups
+    "bias_only_E64": W.small(WL["longtail"], T=700, d=128, H=64).with_(noise=None),
+    "noise_only_E8": W.small(WL["mixtral"], T=500, d=256, H=64).with_(noise="gumbel"),
+    "bias_noise_E6": W.small(WL["longtail"], T=400, d=64, H=64, E=6, k=2),
+    "bias_noise_E50_k3": W.small(WL["longtail"], T=1300, d=128, H=64, E=50, k=3),
 }
+
+
+def test_router_noise_base_not_16_byte_aligned():
+    # a [T, E] noise tensor that starts 4 bytes past a 16-byte boundary (E a
+    # multiple of 4): the router must read it element by element
+    w = W.small(WL["longtail"], T=300, d=128, H=64)
+    inp = W.make_inputs(w)
+    cfg = moe.config_from_workload(w)
+    d = W.to_device(inp, DEV)
+    buf = torch.zeros(w.T * w.E + 4, dtype=torch.float32, device=DEV)
+    noise = buf[1:1 + w.T * w.E].view(w.T, w.E)
+    noise.copy_(d["noise"])
+    assert noise.data_ptr() % 16 == 4
+    lg, idx, gate, psum = moe.router_topk(cfg, d["x"], d["Wg"], d["bias"], noise)
+    lg0, idx0, gate0, psum0 = moe.router_topk(cfg, d["x"], d["Wg"], d["bias"], d["noise"])
+    torch.cuda.synchronize()
+    assert torch.equal(lg, lg0) and torch.equal(idx, idx0)
+    assert torch.equal(gate, gate0) and torch.equal(psum, psum0)
 
 
 @pytest.mark.parametrize("name", sorted(ROUTER_CASES))
