@@ -187,7 +187,7 @@ def bench_config(w, capacity: int, kept: int, n_active: int, nsets: int, fp: int
 
 def time_backward(w, cfg, inp, ws, stream, dev, kept, reps):
     """ms per moe_layer_backward call (loss = sum <dy, y> + 0.01 L_balance),
-    and the tensor-core GEMM work it executes: the recomputed
+    and the GEMM work it executes (tensor cores for bf16, FMA for fp32): the recomputed
     pre-activations (unless cfg keeps them from the forward), dh = dY W2,
     dxd = dact [W1; W3] and the weight gradients, kept * 2 * d * H *
     (3 (nm - 1) + 2) flops, (nm - 1) fewer with kept pre-activations."""
@@ -654,8 +654,9 @@ def main():
     # ---- backward pass of the same layer call (moe_layer_backward), timed
     # alone with CUDA events after one forward call that left its state in ws
     bwd = None
-    if w.dtype == "bf16" and w.shared_H == 0:
+    if w.shared_H == 0:
         bwd = time_backward(w, cfg, sets[0], ws, stream, dev, kept, max(3, args.steps // 20))
+    if w.dtype == "bf16" and w.shared_H == 0:
         # a training forward that keeps the pre-activations, and its backward
         cfg_k = moe.config_from_workload(w, keep_preact=True)
         ws_k = moe.workspace(cfg_k, dev)

@@ -355,8 +355,9 @@ MOE_API moe_status_t moe_workspace_size_backward(const moe_config_t *cfg, size_t
  * expert outputs kept in ws. dy [T, d] is the upstream gradient of y (layer
  * dtype); alpha the weight of L_balance. The expert pre-activations are
  * recomputed (for the activation's derivative). Every sum is taken in
- * a fixed order (results are run-to-run identical). Covered: bf16 (any E);
- * fp32 returns MOE_ERR_UNSUPPORTED. A layer with a shared expert uses
+ * a fixed order (results are run-to-run identical). Covered: bf16 on the
+ * tensor cores and fp32 on fp32 FMA (any E); with fp32 the pre-activations are
+ * always recomputed. A layer with a shared expert uses
  * moe_layer_backward_shared. Nothing is enqueued on a validation failure. */
 MOE_API moe_status_t moe_layer_backward(const moe_config_t *cfg, const moe_layer_inputs_t *in,
                                         const moe_layer_outputs_t *fwd, const void *dy,

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe_b300.so")
 LIB_CHECK = os.path.join(HERE, "libmoe_b300_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_tiles.cu", "dispatch_static.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu", "backward.cu", "ffn_wgrad_tc.cu"]
+SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_tiles.cu", "dispatch_static.cu", "ffn_simt.cu", "ffn_tc.cu", "combine.cu", "backward.cu", "backward_f32.cu", "ffn_wgrad_tc.cu"]
 
 
 def nvcc_path() -> str:

@@ -519,7 +519,7 @@ moe_status_t moe_layer_forward_host_pipelined(const moe_config_t* cfg, const voi
 // ---------------------------------------------------------------- backward
 namespace {
 struct BwdLayout {
-  size_t hdr, pre, dact, dY, dxd, W13T, dz, dg, wg_part, dzb, dxr, goff, wgoff, total;
+  size_t hdr, pre, dact, dY, dxd, W13T, dz, dg, wg_part, dzb, dxr, goff, wgoff, dh, total;
   int kp;  // experts padded to a multiple of 64 (K of the dz W_g GEMM)
 };
 BwdLayout bwd_layout(const moe_config_t& c) {
@@ -527,6 +527,8 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   memset(&L, 0, sizeof(L));
   const size_t R = (size_t)max_rows(c), E = (size_t)c.E, d = (size_t)c.d, H = (size_t)c.H;
   const size_t Hp = c.act == MOE_ACT_SWIGLU ? 2 * H : H;
+  const bool f32 = c.dtype == MOE_F32;
+  const size_t s = f32 ? 4 : 2;  // activation-gradient element bytes
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -535,29 +537,31 @@ BwdLayout bwd_layout(const moe_config_t& c) {
   };
   L.hdr = take(kHdrBytes);
   // recomputed pre-activations, unless the forward kept them in its workspace
-  L.pre = take((c.flags & MOE_FLAG_KEEP_PREACT) ? 0 : R * Hp * 2);
-  L.dact = take(R * Hp * 2);
-  L.dY = take(R * d * 2);
-  L.dxd = take(R * d * 2);
-  L.W13T = take(bwd_w13_transposed(c) ? E * d * Hp * 2 : 0);
+  L.pre = take((c.flags & MOE_FLAG_KEEP_PREACT) ? 0 : R * Hp * s);
+  L.dact = take(R * Hp * s);
+  L.dY = take(R * d * s);
+  L.dxd = take(R * d * s);
+  L.W13T = take(!f32 && bwd_w13_transposed(c) ? E * d * Hp * 2 : 0);
   L.dz = take((size_t)c.T * E * 4);
   L.dg = take((size_t)c.T * (size_t)c.k * 4);
-  L.wg_part = take((size_t)bwd_wg_splits(c) * E * d * 4);
+  L.wg_part = take(f32 ? 0 : (size_t)bwd_wg_splits(c) * E * d * 4);
   L.kp = (int)align_up(E, 64);
-  L.wgoff = take(((size_t)bwd_wg_splits(c) + 1) * 4);
+  L.wgoff = take(f32 ? 0 : ((size_t)bwd_wg_splits(c) + 1) * 4);
   L.dzb = take((size_t)c.T * (size_t)L.kp * 2);
-  L.dxr = take((size_t)c.T * d * 2);
+  L.dxr = take((size_t)c.T * d * s);
   L.goff = take(8);
+  L.dh = take(f32 ? R * H * 4 : 0);  // fp32: dY W2 before the activation's derivative
   L.total = off;
   return L;
 }
-bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16; }
+// bf16 on the tensor cores; fp32 on fp32 FMA (backward_f32.cu)
+bool bwd_supported(const moe_config_t& c) { return c.dtype == MOE_BF16 || c.dtype == MOE_F32; }
 
 // The shared expert's part of the backward workspace, after the routed part:
 // its recomputed pre-activations and activation gradients [T, Hps], its dx
 // term [T, d], the transposed [W1^T | W3^T] where needed, one-group offsets.
 struct BwdSharedLayout {
-  size_t pre, dact, dxs, W13T, soff, total;
+  size_t pre, dact, dxs, W13T, soff, dh, total;
 };
 moe_config_t shared_config(const moe_config_t& c, int H_shared) {
   moe_config_t cs = c;
@@ -578,11 +582,14 @@ BwdSharedLayout bwd_shared_layout(const moe_config_t& c, int H_shared) {
     off += align_up(bytes > 0 ? bytes : 1, 256);
     return at;
   };
-  L.pre = take(T * Hps * 2);
-  L.dact = take(T * Hps * 2);
-  L.dxs = take(T * d * 2);
-  L.W13T = take(bwd_w13_transposed(cs) ? d * Hps * 2 : 0);
+  const bool f32 = c.dtype == MOE_F32;
+  const size_t s = f32 ? 4 : 2;
+  L.pre = take(T * Hps * s);
+  L.dact = take(T * Hps * s);
+  L.dxs = take(T * d * s);
+  L.W13T = take(!f32 && bwd_w13_transposed(cs) ? d * Hps * 2 : 0);
   L.soff = take(8);
+  L.dh = take(f32 ? T * (size_t)H_shared * 4 : 0);
   L.total = off;
   return L;
 }
@@ -595,6 +602,62 @@ moe_status_t moe_workspace_size_backward(const moe_config_t* cfg, size_t* bytes)
   if (!bwd_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
   *bytes = bwd_layout(*cfg).total;
   return MOE_OK;
+}
+
+// The fp32 backward: the steps of the bf16 one on fp32 FMA, reading what the
+// fp32 forward left in its workspace (gathered rows xd, hidden rows h, expert
+// outputs Y for k > 1; the shared expert's hidden rows).
+static cudaError_t layer_backward_f32(const moe_config_t& c, const moe_layer_inputs_t* in,
+                                      const moe_shared_expert_t* sh,
+                                      const moe_layer_outputs_t* fwd, const float* dy,
+                                      float alpha, const moe_layer_grads_t* g,
+                                      const moe_shared_grads_t* sg, void* ws, const WsLayout& L,
+                                      void* bws, const BwdLayout& B, const BwdSharedLayout& BS,
+                                      cudaStream_t s) {
+  const int64_t R = max_rows(c);
+  const float* xd = at<float>(ws, L.xd);
+  const float* Y = c.k > 1 ? at<float>(ws, L.Y) : nullptr;  // k = 1: gates are identically 1
+  const int32_t* off = fwd->expert_offset;
+  float* dYb = at<float>(bws, B.dY);
+  float* dz = at<float>(bws, B.dz);
+  float* dg = at<float>(bws, B.dg);
+  float* dxr = at<float>(bws, B.dxr);
+  float* dxd = at<float>(bws, B.dxd);
+  int32_t* goff = at<int32_t>(bws, B.goff);
+  cudaError_t e = launch_bwdf_combine(c, dy, Y, fwd->slot_of, fwd->topk_gate, dYb, dg, s);
+  if (e == cudaSuccess)
+    e = launch_bwd_router(c, fwd->logits, fwd->topk_idx, fwd->topk_gate, dg, fwd->f, alpha, dz,
+                          at<void>(bws, B.dzb), B.kp, s);
+  if (e == cudaSuccess) e = launch_one_group_offsets(goff, c.T, s);
+  if (e == cudaSuccess)
+    e = launch_router_grads_f32(c, dz, static_cast<const float*>(in->x),
+                                static_cast<const float*>(in->Wg), goff, g->dWg, g->dbias, dxr, s);
+  if (e == cudaSuccess)
+    e = launch_expert_bwd_f32(c, xd, off, R, static_cast<const float*>(in->W1),
+                              static_cast<const float*>(in->W3), static_cast<const float*>(in->b1),
+                              static_cast<const float*>(in->W2), dYb, at<float>(ws, L.ffn_h),
+                              at<float>(bws, B.pre), at<float>(bws, B.dh), at<float>(bws, B.dact),
+                              dxd, g->dW1, g->dW3, g->dW2, g->db1, g->db2, s);
+  // the shared expert: one group of all T token rows, output gradient dy
+  float* dxs = nullptr;
+  if (sh && e == cudaSuccess) {
+    const moe_config_t cs = shared_config(c, sh->H);
+    int32_t* soff = at<int32_t>(bws, BS.soff);
+    dxs = at<float>(bws, BS.dxs);
+    e = launch_one_group_offsets(soff, c.T, s);
+    if (e == cudaSuccess)
+      e = launch_expert_bwd_f32(cs, static_cast<const float*>(in->x), soff, c.T,
+                                static_cast<const float*>(sh->W1),
+                                static_cast<const float*>(sh->W3),
+                                static_cast<const float*>(sh->b1),
+                                static_cast<const float*>(sh->W2), dy, at<float>(ws, L.sh_h),
+                                at<float>(bws, BS.pre), at<float>(bws, BS.dh),
+                                at<float>(bws, BS.dact), dxs, sg->dW1, sg->dW3, sg->dW2, sg->db1,
+                                sg->db2, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_bwdf_dx(c, dxr, dxd, dxs, fwd->slot_of, static_cast<float*>(g->dx), s);
+  return e;
 }
 
 static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer_inputs_t* in,
@@ -635,6 +698,9 @@ static moe_status_t layer_backward_impl(const moe_config_t* cfg, const moe_layer
   const BwdSharedLayout BS = bwd_shared_layout(c, Hs > 0 ? Hs : 8);
   if ((st = check_ws(bws, bws_bytes, sh ? BS.total : B.total)) != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  if (c.dtype == MOE_F32)
+    return cuda_status(layer_backward_f32(c, in, sh, fwd, static_cast<const float*>(dy), alpha,
+                                          g, sg, const_cast<void*>(ws), L, bws, B, BS, s));
   const int64_t R = max_rows(c);
   const int Hp = swiglu ? 2 * c.H : c.H;
   int32_t* hdr = at<int32_t>(bws, 0);
@@ -728,7 +794,7 @@ moe_status_t moe_workspace_size_backward_shared(const moe_config_t* cfg, int32_t
                                                 size_t* bytes) {
   const moe_status_t st = validate(cfg);
   if (st != MOE_OK) return st;
-  if (!bytes || H_shared < 1 || H_shared % 8) return MOE_ERR_INVALID_ARG;
+  if (!bytes || H_shared < 1 || H_shared % (cfg->dtype == MOE_F32 ? 4 : 8)) return MOE_ERR_INVALID_ARG;
   if (!bwd_supported(*cfg)) return MOE_ERR_UNSUPPORTED;
   *bytes = bwd_shared_layout(*cfg, H_shared).total;
   return MOE_OK;

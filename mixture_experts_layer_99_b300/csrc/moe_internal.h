@@ -268,6 +268,21 @@ cudaError_t launch_weight_transpose(const void* in, int E, int A, int B, int ld_
                                     void* out, cudaStream_t s);
 cudaError_t launch_expert_colsum(const void* a, int ld, int C, const int32_t* off, int E,
                                  float* out, cudaStream_t s);
+// fp32 backward (backward_f32.cu): fp32 FMA throughout
+cudaError_t launch_expert_bwd_f32(const moe_config_t& c, const float* xd, const int32_t* off,
+                                  int64_t rows_bound, const float* W1, const float* W3,
+                                  const float* b1, const float* W2, const float* dY,
+                                  const float* h, float* pre, float* dh, float* dact, float* dxd,
+                                  float* dW1, float* dW3, float* dW2, float* db1, float* db2,
+                                  cudaStream_t s);
+cudaError_t launch_bwdf_combine(const moe_config_t& c, const float* dy, const float* Y,
+                                const int32_t* slot_of, const float* gate, float* dY, float* dg,
+                                cudaStream_t s);
+cudaError_t launch_router_grads_f32(const moe_config_t& c, const float* dz, const float* x,
+                                    const float* Wg, const int32_t* one_group_off, float* dWg,
+                                    float* dbias, float* dxr, cudaStream_t s);
+cudaError_t launch_bwdf_dx(const moe_config_t& c, const float* dxr, const float* dxd,
+                           const float* dxs, const int32_t* slot_of, float* dx, cudaStream_t s);
 cudaError_t launch_aux(const moe_config_t& c, const int32_t* count, const float* prob_sum,
                        const float* partial, int nparts, float* f, float* P, float* L,
                        int32_t* dropped, cudaStream_t s);
