@@ -145,11 +145,12 @@ inline int router_tc_grid(const moe_config_t& c) {
 struct RouterSplit {
   int ksplit, kb_per_split;
 };
+constexpr int kRouterMaxSplit = 8;  // CTAs of a split cluster (portable cluster size)
 inline RouterSplit router_tc_split(const moe_config_t& c) {
   const int tiles = router_tc_tiles(c);
   const int num_kb = (c.d + 63) / 64;
   if (tiles > 16) return RouterSplit{1, num_kb};
-  int want = 8;
+  int want = kRouterMaxSplit;
   if (want > num_kb) want = num_kb;
   const int per = (num_kb + want - 1) / want;
   return RouterSplit{(num_kb + per - 1) / per, per};

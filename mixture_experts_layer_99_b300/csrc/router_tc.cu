@@ -663,12 +663,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (warp >= 2 && item < BM * nv) {
         row4[it] = item / nv;
         col4[it] = c0 + 4 * (item % nv);
-        for (int qq = 0; qq < ksplit; ++qq) {
-          const float4 w = ld_cluster_v4(cluster_addr(&st.epi.L[row4[it]][col4[it]], (uint32_t)qq));
-          acc4[it].x += w.x;
-          acc4[it].y += w.y;
-          acc4[it].z += w.z;
-          acc4[it].w += w.w;
+        // every rank's piece in flight at once, then summed in split order
+        // (added one by one after each load, the eight remote round trips
+        // ran back to back)
+        float4 w[kRouterMaxSplit];
+#pragma unroll
+        for (int qq = 0; qq < kRouterMaxSplit; ++qq)
+          if (qq < ksplit)
+            w[qq] = ld_cluster_v4(cluster_addr(&st.epi.L[row4[it]][col4[it]], (uint32_t)qq));
+#pragma unroll
+        for (int qq = 0; qq < kRouterMaxSplit; ++qq) {
+          if (qq < ksplit) {
+            acc4[it].x += w[qq].x;
+            acc4[it].y += w[qq].y;
+            acc4[it].z += w[qq].z;
+            acc4[it].w += w[qq].w;
+          }
         }
       }
     }
