@@ -19,6 +19,10 @@
 namespace moe {
 namespace {
 
+// Rounds of 32 slots a warp owns: 128 / 8 tokens of k <= 8 slots.
+constexpr int kIdsPerLane = 4;
+static_assert(kRouterTcTile / 8 * kMaxK <= 32 * kIdsPerLane, "slots per warp");
+
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -64,6 +68,19 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
   const int tile = blockIdx.x;
   for (int i = tid; i < 8 * kMaxE; i += 256) (&wcnt[0][0])[i] = 0;
   pdl_wait();
+  // this warp's slots of the tile: rows/8 tokens (rows <= 128), k slots each,
+  // at most kIdsPerLane rounds of 32. Their expert ids are loaded now, so that
+  // the loads overlap the tile-count sums instead of following them.
+  const int64_t nslots = (int64_t)T * k;
+  const int wrows = rows / 8;                                   // tokens per warp
+  const int64_t s0 = ((int64_t)tile * rows + (int64_t)wrows * w) * k;  // first slot of this warp
+  const int per_warp = wrows * k;
+  int ids[kIdsPerLane];
+#pragma unroll
+  for (int r = 0; r < kIdsPerLane; ++r) {
+    const int64_t s = s0 + 32 * r + lane;
+    ids[r] = (32 * r + lane < per_warp && s < nslots) ? idx[s] : -1;
+  }
   {
     // partial sums per (group g, expert e) into wcnt, as [2][G][E] ints
     // (G E <= 1024), then tot/base per expert
@@ -196,14 +213,9 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
     }
   }
   // ---- stable positions within the tile
-  const int64_t nslots = (int64_t)T * k;
-  const int wrows = rows / 8;                                   // tokens per warp
-  const int64_t s0 = ((int64_t)tile * rows + (int64_t)wrows * w) * k;  // first slot of this warp
-  const int per_warp = wrows * k;
-  for (int c = 0; c < per_warp; c += 32) {
-    const int64_t s = s0 + c + lane;
-    const bool in = (c + lane < per_warp) && s < nslots;
-    const int e = in ? idx[s] : -1;
+#pragma unroll
+  for (int r = 0; r < kIdsPerLane; ++r) {
+    const int e = ids[r];
     if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[w][e], 1);
   }
   __syncthreads();
@@ -218,10 +230,13 @@ __global__ void __launch_bounds__(256) dispatch_tiles_kernel(
   }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
-  for (int c = 0; c < per_warp; c += 32) {
+#pragma unroll
+  for (int r = 0; r < kIdsPerLane; ++r) {
+    const int c = 32 * r;
+    if (c >= per_warp) break;
     const int64_t s = s0 + c + lane;
     const bool in = (c + lane < per_warp) && s < nslots;
-    int e = in ? idx[s] : -1;
+    int e = in ? ids[r] : -1;
     const bool valid = (unsigned)e < (unsigned)E;
     if (!valid) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
