@@ -53,9 +53,13 @@ __device__ __forceinline__ uint4 pack(const float (&f)[8], float*) {
 // lines, so they come from the cache) and adds nothing, which keeps every
 // load unconditional and in flight together. A token without a kept slot
 // writes its base row, or zeros.
+// Two vectors per lane and slot for k <= 2: measured on B300 (layer call,
+// alternating builds, identical outputs) the combine took 50.8 us on the long
+// tail and 72.3 us on mixtral with two, 55.5 / 77.7 us with four, 54 / 78 us
+// with one and 77 / 110 us with eight.
 template <int KM>
 struct CombineShape {
-  static constexpr int UNR = KM <= 2 ? 4 : (KM <= 4 ? 2 : 1);
+  static constexpr int UNR = KM <= 2 ? 2 : (KM <= 4 ? 2 : 1);
   static constexpr int CHUNK = 32 * UNR;
 };
 template <typename T, int KM>
