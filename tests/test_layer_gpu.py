@@ -35,6 +35,11 @@ SMALL = {
     "std_noise_small": W.small(WL["sweep_std_noise"], T=2048, d=256, H=512),
     # 157 router tiles in two rounds over the 148 CTAs, with drops
     "tiles_two_rounds": W.small(WL["longtail"], T=20000, d=128, H=64),
+    # fp32 beyond the reference layer: SwiGLU with router bias, Gumbel noise
+    # and drops over 64 experts; 96 experts top-4 (the FMA router)
+    "f32_swiglu_drops": W.small(WL["longtail"], T=700, d=64, H=96).with_(dtype="f32"),
+    "f32_wide_e96_k4": W.small(WL["switch_top1"], T=500, d=64, H=64, E=96,
+                               k=4).with_(dtype="f32"),
 }
 
 
