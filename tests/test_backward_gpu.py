@@ -54,6 +54,11 @@ CASES = {
                                 k=4).with_(dtype="f32"), 0.05, False),
     "f32_bias_noise_tau": (W.small(WL["longtail"], T=500, d=64, H=64).with_(dtype="f32",
                                                                            tau=0.7), 0.1, False),
+    # fp32 dimensions that are not multiples of the 64-wide GEMM tiles
+    "f32_ragged_dims": (W.small(WL["switch_top1"], T=333, d=36, H=52, E=5,
+                                k=2).with_(dtype="f32"), 0.2, True),
+    "f32_ragged_swiglu": (W.small(WL["mixtral"], T=211, d=44, H=28, E=3).with_(dtype="f32"),
+                          0.2, False),
 }
 
 
