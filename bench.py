@@ -300,10 +300,11 @@ def run_reference(args, w):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    # the sample is sized like the GPU arm's cpu_baseline (a few seconds per
-    # call): at a few dozen tokens the oracle's fixed cost (each expert's
-    # weights converted to fp64) would dominate its per-token rate
-    per_step = time_oracle(w, target_s=12.0)
+    # each step is a sample of about three seconds of oracle work (so that a
+    # run of 20 + 5 steps ends in a couple of minutes): at a few dozen tokens
+    # the oracle's fixed cost (each expert's weights converted to fp64) would
+    # dominate its per-token rate
+    per_step = time_oracle(w, target_s=6.0)
     n = per_step["tokens"]
     from oracle import moe_oracle as ORC
     inp = W.make_inputs(w)
